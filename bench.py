@@ -1,0 +1,500 @@
+"""Benchmark of the FP8 block-scaled GEMM hot path on GB300.
+
+One step = one pass of the whole hot path over every full-size workload: for each of
+  decode           dense  M=64,   N=7168, K=7168
+  large_4096       dense  M=N=K=4096
+  large_4096x8192  dense  M=4096, N=8192, K=8192
+  moe_contiguous   grouped, 4096 tokens top-2 over 8 experts (rows padded to 128), N=4096, K=7168
+  moe_masked       grouped, 32 experts x capacity 256, valid rows ~U{0..256}, N=4096, K=7168
+quantise the bf16 activations (1x128, on the GPU) and run the GEMM.  Weights are
+quantised (128x128) once, before timing, as model weights would be.  L2 is flushed (a
+512 MB write) before each workload, outside the timed brackets.
+
+metric: FP8 block-scaled GEMM TFLOP/s = sum of 2*M*N*K over valid rows / device time of
+the step (CUDA events on the launching stream).  The line also carries the dominant
+kernel's roofline, a CPU baseline (the numpy oracle on a bounded sample, host cores),
+an end-to-end figure through the public API with host buffers, sampled clocks and the
+number of library kernels launched.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workloads a,b]
+Multi-GPU: one process per GPU under torchrun; every rank runs an independent replica
+(the path has no exchange step), timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_grouped_gemm_block_gb300.workloads import WORKLOADS, gemm_flops, make_inputs  # noqa: E402
+
+METRIC = "FP8 block-scaled GEMM TFLOPS (dense + MoE grouped), % of GB300 FP8 peak"
+DEFAULT_WORKLOADS = ["decode", "large_4096", "large_4096x8192", "moe_contiguous", "moe_masked"]
+FLUSH_BYTES = 512 << 20
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def maybe_init_pg(world: int):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path:
+                try:
+                    os.unlink(self.path)
+                except OSError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Case:
+    """Device-resident inputs and outputs of one workload; `run()` enqueues its hot path."""
+
+    def __init__(self, name: str, g, dev):
+        self.name = name
+        self.w = w = WORKLOADS[name]
+        self.g = g
+        inp = make_inputs(w, dev)
+        self.flops = gemm_flops(w, inp)
+        A = inp["A"].reshape(-1, w.K)
+        self.A = A
+        self.rows = A.shape[0]
+        self.qA = torch.empty((self.rows, w.K), dtype=torch.uint8, device=dev)
+        ld_sa = (self.rows + 3) // 4 * 4
+        self.sA = torch.empty((w.K // 128, ld_sa), dtype=torch.float32, device=dev)
+        self.qB, self.sB = g.quantize_128x128(inp["B"])  # offline weight quantisation (untimed)
+        del inp["B"]
+        if w.kind == "dense":
+            self.D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+            self.meta = None
+        elif w.kind == "contiguous":
+            self.D = torch.empty((self.rows, w.N), dtype=torch.bfloat16, device=dev)
+            self.meta = inp["group_offsets"].to(dev)
+        else:
+            self.D = torch.empty((w.E, w.cap, w.N), dtype=torch.bfloat16, device=dev)
+            self.meta = inp["masked_m"].to(dev)
+        self.masked_rows = int(inp["masked_m"].sum()) if w.kind == "masked" else None
+        # algorithmic bytes: quantise reads bf16 A, writes e4m3 A + scales
+        self.q_bytes = self.rows * w.K * 3 + self.rows * (w.K // 128) * 4
+        self.gemm_bytes = self._gemm_bytes()
+
+    def _gemm_bytes(self) -> float:
+        w = self.w
+        kb = w.K // 128
+        nbs = (w.N + 127) // 128
+        if w.kind == "dense":
+            return w.M * w.K + w.N * w.K + 4 * (w.M * kb + nbs * kb * w.E) + 2 * w.M * w.N
+        if w.kind == "contiguous":
+            return self.rows * w.K + w.E * w.N * w.K + 4 * (self.rows * kb + w.E * nbs * kb) + 2 * self.rows * w.N
+        m = self.masked_rows
+        active = int((self.meta > 0).sum())
+        return m * w.K + active * w.N * w.K + 4 * (m * kb + active * nbs * kb) + 2 * m * w.N
+
+    def quantize(self, A=None):
+        self.g.fp8_quantize_1x128(self.A if A is None else A, self.qA, self.sA)
+
+    def gemm(self, D=None):
+        g, w = self.g, self.w
+        D = self.D if D is None else D
+        if w.kind == "dense":
+            g.fp8_gemm_nt(self.qA, self.sA, self.qB, self.sB, D)
+        elif w.kind == "contiguous":
+            g.fp8_grouped_gemm_contiguous(self.qA, self.sA, self.qB, self.sB, D, self.meta)
+        else:
+            g.fp8_grouped_gemm_masked(self.qA.view(w.E, w.cap, w.K), self.sA, self.qB, self.sB, D, self.meta)
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_grouped_gemm_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            for line in f:
+                parts = line.split("#")[0].split()
+                if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == source_digest():
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+def run_ours(args, world, rank, local, dist):
+    import moe_grouped_gemm_block_gb300 as g
+
+    if not os.path.exists(g.LIB_PATH):
+        from moe_grouped_gemm_block_gb300.build import build
+        build()
+    g.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    names = args.workloads
+    cases = [Case(n, g, dev) for n in names]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    if g.fp8g_get_status() != 0:
+        raise RuntimeError("device status not OK after setup")
+
+    def one_step(record):
+        for i, c in enumerate(cases):
+            flush.fill_(i & 0xFF)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            c.quantize()
+            ev[1].record(stream)
+            c.gemm()
+            ev[2].record(stream)
+            record.append((c.name, ev))
+
+    for _ in range(args.warmup):
+        one_step([])
+    torch.cuda.synchronize()
+
+    launches_per_step = 2 * len(cases)
+    records = []
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            one_step(records)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(dist)
+    st = g.fp8g_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {g.STATUS.get(st, st)} after the timed region")
+
+    per = {n: {"q": [], "g": []} for n in names}
+    for n, ev in records:
+        per[n]["q"].append(ev[0].elapsed_time(ev[1]))
+        per[n]["g"].append(ev[1].elapsed_time(ev[2]))
+    step_ms = sum(sum(per[n]["q"]) + sum(per[n]["g"]) for n in names) / args.steps
+    step_ms = max_over_ranks(step_ms, dist)
+    flops_step = sum(c.flops for c in cases)
+    value = world * flops_step / (step_ms * 1e-3) / 1e12
+
+    pk, pk_kind = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]  # dense e4m3 = 2 x dense bf16 (nominal 4.5 / 2.25 PFLOP/s)
+    hbm_peak = pk["hbm_gbs"]
+    breakdown = {}
+    kernels = []
+    for c in cases:
+        qm = statistics.mean(per[c.name]["q"])
+        gm = statistics.mean(per[c.name]["g"])
+        tf = c.flops / (gm * 1e-3) / 1e12
+        breakdown[c.name] = {
+            "gemm_us": round(gm * 1e3, 2), "quant_us": round(qm * 1e3, 2),
+            "gemm_tflops": round(tf, 1), "pct_fp8_peak": round(100 * tf / fp8_peak, 1),
+            "gemm_gbs": round(c.gemm_bytes / (gm * 1e-3) / 1e9, 1),
+            "pct_hbm_peak": round(100 * c.gemm_bytes / (gm * 1e-3) / 1e9 / hbm_peak, 1),
+            "quant_gbs": round(c.q_bytes / (qm * 1e-3) / 1e9, 1),
+        }
+        kernels.append(("gemm:" + c.name, sum(per[c.name]["g"]), c, "gemm", gm))
+        kernels.append(("quant:" + c.name, sum(per[c.name]["q"]), c, "quant", qm))
+    top = max(kernels, key=lambda k: k[1])
+    key, _, c, kind, avg_ms = top
+    if kind == "gemm":
+        roof = {"kernel": f"fp8_gemm_kernel ({c.name})", "bound": "tensor", "achieved": c.flops / (avg_ms * 1e-3) / 1e12,
+                "peak": fp8_peak, "unit": "TFLOP/s", "peak_source": f"2 x bf16_tflops ({pk_kind})"}
+    else:
+        roof = {"kernel": f"quantize_1x128_kernel ({c.name})", "bound": "hbm",
+                "achieved": c.q_bytes / (avg_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "peak_source": f"hbm_gbs ({pk_kind})"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["achieved"] = round(roof["achieved"], 2)
+    roof["frac"] = round(roof["frac"], 4)
+    roof["traffic"] = traffic_for(key)
+    roof["share"] = round(top[1] / sum(k[1] for k in kernels), 3)
+
+    e2e = measure_e2e(cases, g, dev, max(2, min(args.steps, 5)), dist, world)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded normal draws; outlier channels; softmax top-2 routing; uniform masked counts)",
+        "config": {"workload": "+".join(names), "parallelism": f"replicas{world}",
+                   "l2": "flushed (512 MB write) before every workload, outside the timed brackets",
+                   "accumulate": "fp32", "out": "bf16", "scales": "1x128 (A), 128x128 (B)"},
+        "pct_fp8_peak": round(100 * value / world / fp8_peak, 2),
+        "per_workload": breakdown,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+        "source": source_digest(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(names, target_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def measure_e2e(cases, g, dev, steps, dist, world):
+    """Same metric through the public API with host buffers: pinned bf16 activations (and the
+    routing metadata) copied in, the bf16 result copied out, inside the timed region."""
+    stream = torch.cuda.current_stream()
+    host_in = [c.A.cpu().pin_memory() for c in cases]
+    host_meta = [c.meta.cpu().pin_memory() if c.meta is not None else None for c in cases]
+    host_out = [torch.empty(c.D.shape, dtype=c.D.dtype).pin_memory() for c in cases]
+    dev_in = [torch.empty_like(c.A) for c in cases]
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + sum(
+        t.numel() * t.element_size() for t in host_meta if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for c, hi, hm, ho, di in zip(cases, host_in, host_meta, host_out, dev_in):
+            di.copy_(hi, non_blocking=True)
+            if hm is not None:
+                c.meta.copy_(hm, non_blocking=True)
+            c.quantize(di)
+            c.gemm()
+            ho.copy_(c.D, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist)
+    flops = sum(c.flops for c in cases)
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "weights resident (quantised once); activations + routing metadata in, bf16 result out"}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def oracle_sample(names, scale=1.0):
+    """Bounded sample of every workload for the CPU oracle: `rows` activation rows against
+    `cols` weight rows (whole 128-row weight blocks).  Inputs are drawn on the CPU."""
+    from oracle import quantize_128x128
+
+    samples = []
+    for n in names:
+        w = WORKLOADS[n]
+        g = torch.Generator().manual_seed(w.seed)
+        rows = max(8, int(64 * scale))
+        cols = 128 * max(1, int(8 * scale))
+        a = (torch.randn((rows, w.K), generator=g) * 1.0).to(torch.bfloat16).float().numpy()
+        std = 1.0 if w.b_std_one else 1.0 / np.sqrt(w.K)
+        b = (torch.randn((cols, w.K), generator=g) * std).to(torch.bfloat16).float().numpy()
+        qb, sb = quantize_128x128(b)  # weight preparation: not timed
+        samples.append((n, a, qb, sb, 2.0 * rows * cols * w.K))
+    return samples
+
+
+def time_oracle(samples):
+    from oracle import gemm_nt, quantize_1x128
+
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _, a, qb, sb, f in samples:
+        qa, sa = quantize_1x128(a)
+        gemm_nt(qa, sa, qb, sb)
+        flops += f
+    return flops, time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(names, target_s=15.0):
+    samples = oracle_sample(names)
+    flops, dt = time_oracle(samples)  # first pass: also calibrates the repeat count
+    reps = max(1, int(target_s / max(dt, 1e-3)))
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(reps):
+        f, t = time_oracle(samples)
+        tot_f += f
+        tot_t += t
+    return {"value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} passes over 64 rows x 1024 weight rows of each of {', '.join(names)} "
+                      f"(1x128 quantise + blockwise GEMM, numpy fp64 block dots)",
+            "seconds": round(tot_t, 2)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    samples = oracle_sample(args.workloads)
+    for _ in range(args.warmup):
+        time_oracle(samples)
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t = time_oracle(samples)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block dots, f32 promotion",
+        "data": "synthetic", "config": {"workload": "+".join(args.workloads), "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": "each step: 64 rows x 1024 weight rows of every workload"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workloads", default=",".join(DEFAULT_WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.workloads = [w for w in args.workloads.split(",") if w]
+    for w in args.workloads:
+        if w not in WORKLOADS:
+            raise SystemExit(f"unknown workload {w}")
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    dist = maybe_init_pg(world)
+    try:
+        run_ours(args, world, rank, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

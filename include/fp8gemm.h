@@ -1,0 +1,176 @@
+/*
+ * fp8gemm.h -- C ABI of the GB300 (sm_103a) FP8 block-scaled GEMM library.
+ *
+ * What is computed.  FP8 e4m3 operands with fine-grained block scales, FP32
+ * accumulation and a BF16 result:
+ *
+ *     D[m, n] = bf16( sum_kb  P_kb[m, n] * sA[kb][m] * sB[n / 128][kb] )
+ *     P_kb[m, n] = sum_{k in K block kb} A[m, k] * B[n, k]       (128-wide K blocks)
+ *
+ * Sources (page title, section):
+ *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
+ *    scales for the activations A, per-channel scales for the weights B, K cut
+ *    into blocks; scales handled inside the GEMM pipeline.  Sec. 2.3: FP32
+ *    accumulation across the whole K, rounding to the output type only on write.
+ *  - "DeepGEMM explainer" (nxmr.cn/news/131680), sec. 3.1: a block's scale is its
+ *    amax divided by the largest FP8 value; sec. 3.2: the MoE grouped GEMM runs
+ *    experts with different token counts in one kernel; sec. 3.3: operands are
+ *    taken without a transpose (A and B both K-contiguous, "NT"); sec. 4.2: the
+ *    call takes FP8 a and b, their scales and the group sizes; sec. 5.1: the
+ *    scale shapes must match the blocking (1x128 rows of A, 128x128 blocks of B).
+ *  - "Production FP8 GEMM alignment and Tensor Core peak tuning" (gtnt.cn/news/117510),
+ *    "E4M3 vs E5M2": e4m3 range +-448.
+ *
+ * Conventions for every call:
+ *  - Every pointer is CUDA device memory on the current device, owned by the
+ *    caller.  The library never allocates, frees or synchronises caller
+ *    buffers, and never synchronises the stream (except fp8g_get_status).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Work is enqueued on it; results are valid once the stream reaches that point.
+ *  - The return value is an fp8g_status.  Arguments are validated on the host
+ *    before anything is launched; an invalid call launches nothing and returns
+ *    FP8G_ERR_INVALID_ARG or FP8G_ERR_ALIGNMENT.  Calls never throw.
+ *  - Errors found on the device (a bounded wait that ran out, out-of-contract
+ *    group offsets or counts) are recorded in a per-device status word that
+ *    fp8g_get_status reads and clears; the kernel returns early instead of
+ *    trapping, so the CUDA context stays usable.
+ *  - e4m3 bytes use the OCP "e4m3fn" encoding (no infinities, 0x7F/0xFF NaN,
+ *    max 448).  Inputs must be finite.
+ *  - Only sm_103 devices are supported; anything else returns
+ *    FP8G_ERR_UNSUPPORTED_DEVICE (there is no fallback path).
+ *  - Calls are thread-safe; calls on different streams may run concurrently.
+ */
+#ifndef FP8GEMM_H_
+#define FP8GEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8G_OK = 0,
+  FP8G_ERR_INVALID_ARG = 1,        /* a size, count or leading dimension out of range */
+  FP8G_ERR_ALIGNMENT = 2,          /* a pointer or stride not 16-byte aligned */
+  FP8G_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
+  FP8G_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (launch, attribute, ...) */
+  FP8G_ERR_TIMEOUT = 5,            /* device: a pipeline wait ran past its cycle budget */
+  FP8G_ERR_DEVICE_ASSERT = 6       /* device: out-of-contract group offsets / masked counts */
+} fp8g_status;
+
+/*
+ * fp8_quantize_1x128 -- activation quantisation, one scale per row and 128-wide
+ * K block ("DeepGEMM explainer" sec. 3.1; "DeepGEMM FP8 walk-through" sec. 5.2).
+ *
+ * For every row m and block kb (columns 128*kb .. 128*kb+127):
+ *     amax = max |x|;  s = fp32(amax / 448);  q = e4m3(fp32(x / s))
+ * with IEEE fp32 division, round-to-nearest-even, saturation to +-448 and the
+ * sign kept.  A block with amax == 0 gets s = 0 and all codes 0x00.
+ *
+ *   x     bf16 [M, K], row stride ldx elements (ldx >= K, ldx % 8 == 0)
+ *   q     e4m3 [M, K] (one byte each), row stride ldq bytes (ldq >= K, ldq % 16 == 0)
+ *   sA    fp32 [K/128][ld_sa], K-block-major: sA[kb * ld_sa + m]
+ *         (ld_sa >= M, ld_sa % 4 == 0; entries m >= M are not written)
+ *   M >= 0 (M == 0: no-op), K > 0, K % 128 == 0.  Pointers 16-byte aligned.
+ */
+int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                       float* sA, int64_t ld_sa, void* stream);
+
+/*
+ * fp8_quantize_128x128 -- weight quantisation, one scale per 128x128 block
+ * ("DeepGEMM explainer" sec. 5.1; "DeepGEMM FP8 walk-through" sec. 2.2).
+ * Same rule as fp8_quantize_1x128 with amax taken over the block's rows that
+ * exist (N need not be a multiple of 128).
+ *
+ *   w     bf16 [E, N, K], contiguous
+ *   q     e4m3 [E, N, K], contiguous
+ *   sB    fp32 [E][ceil(N/128)][K/128], contiguous
+ *   E >= 1, N >= 1, K > 0, K % 128 == 0.  Pointers 16-byte aligned.
+ */
+int fp8_quantize_128x128(const void* w, int64_t E, int64_t N, int64_t K, void* q, float* sB,
+                         void* stream);
+
+/*
+ * fp8_gemm_nt -- dense D = A * B^T with 1x128 scales on A and 128x128 scales on B
+ * ("DeepGEMM FP8 walk-through" sec. 2.2-2.3; "DeepGEMM explainer" sec. 3.3).
+ *
+ *   A     e4m3 [M, K], row stride lda bytes (lda >= K, lda % 16 == 0)
+ *   sA    fp32 [K/128][ld_sa] (ld_sa >= M, ld_sa % 4 == 0), as written by fp8_quantize_1x128
+ *   B     e4m3 [N, K], row stride ldb bytes (ldb >= K, ldb % 16 == 0)
+ *   sB    fp32 [ceil(N/128)][K/128], contiguous
+ *   D     bf16 [M, N], row stride ldd elements (ldd >= N, ldd % 8 == 0)
+ *   M >= 0 (M == 0: no-op), N > 0, N % 16 == 0, K > 0, K % 128 == 0.
+ */
+int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa, const void* B,
+                int64_t ldb, const float* sB, void* D, int64_t ldd, int64_t M, int64_t N,
+                int64_t K, void* stream);
+
+/*
+ * fp8_grouped_gemm_contiguous -- MoE grouped GEMM, contiguous layout
+ * ("DeepGEMM explainer" sec. 3.2 and 4.2; "DeepGEMM FP8 walk-through" sec. 5.3:
+ * pass each group's id and token offset; keep each expert's rows contiguous and
+ * block-loadable).  Expert e owns rows group_offsets[e] .. group_offsets[e+1]-1
+ * of A and D:
+ *     D[rows of e] = gemm_nt(A[rows of e], B[e])
+ * Rows that belong to no group are left untouched.  Padding rows inside a
+ * group are computed like any other row (all-zero rows give zeros).
+ *
+ *   A             e4m3 [M_total, K], contiguous
+ *   sA            fp32 [K/128][ld_sa] (ld_sa >= M_total, ld_sa % 4 == 0)
+ *   B             e4m3 [E, N, K], contiguous
+ *   sB            fp32 [E][ceil(N/128)][K/128], contiguous
+ *   D             bf16 [M_total, N], contiguous
+ *   group_offsets int32 [E+1], DEVICE memory, read only by the kernel (the host
+ *                 never reads it, so routing can stay on the GPU): non-decreasing,
+ *                 each a multiple of 128, group_offsets[E] <= M_total.  Violations
+ *                 make the kernel write nothing and set FP8G_ERR_DEVICE_ASSERT.
+ *   1 <= E <= 4096, M_total >= 0 and M_total % 128 == 0, N % 16 == 0, K % 128 == 0.
+ */
+int fp8_grouped_gemm_contiguous(const void* A, const float* sA, int64_t ld_sa, const void* B,
+                                const float* sB, void* D, const int32_t* group_offsets,
+                                int32_t E, int64_t M_total, int64_t N, int64_t K, void* stream);
+
+/*
+ * fp8_grouped_gemm_masked -- MoE grouped GEMM, masked layout: every expert has
+ * a fixed capacity of rows and a device-side count of valid rows.  (The pages
+ * describe the grouped GEMM but not this layout; it is the decode-time form in
+ * which the per-expert token counts stay on the GPU.)
+ *     D[e, m, :] = gemm_nt(A[e, m, :], B[e])   for m < masked_m[e]
+ * Rows m >= masked_m[e] of D are never written.
+ *
+ *   A         e4m3 [E, cap, K], contiguous
+ *   sA        fp32 [K/128][ld_sa] with row index e*cap + m (ld_sa >= E*cap, ld_sa % 4 == 0)
+ *   B         e4m3 [E, N, K], contiguous
+ *   sB        fp32 [E][ceil(N/128)][K/128], contiguous
+ *   D         bf16 [E, cap, N], contiguous
+ *   masked_m  int32 [E], DEVICE memory, 0 <= masked_m[e] <= cap; values outside are
+ *             clamped into range and set FP8G_ERR_DEVICE_ASSERT.
+ *   1 <= E <= 4096, cap >= 0 and cap % 16 == 0, N % 16 == 0, K % 128 == 0.
+ */
+int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t ld_sa, const void* B,
+                            const float* sB, void* D, const int32_t* masked_m, int32_t E,
+                            int64_t cap, int64_t N, int64_t K, void* stream);
+
+/*
+ * fp8g_get_status -- synchronise `stream`, then return and clear the current
+ * device's status word (FP8G_OK if no kernel recorded an error since the last
+ * call).  Returns FP8G_ERR_CUDA if the synchronisation itself fails.
+ */
+int fp8g_get_status(void* stream);
+
+/* fp8g_status_string -- a static, human-readable name for a status code. */
+const char* fp8g_status_string(int code);
+
+/*
+ * fp8g_last_config -- the tile configuration the last GEMM call on this thread
+ * launched: block N (columns per tile), pipeline stages and grid size.
+ * Diagnostic only; returns FP8G_OK, or FP8G_ERR_INVALID_ARG for null pointers.
+ */
+int fp8g_last_config(int* block_n, int* stages, int* grid);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GEMM_H_ */

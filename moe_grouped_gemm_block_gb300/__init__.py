@@ -1,0 +1,209 @@
+"""FP8 e4m3 block-scaled GEMM for GB300 (sm_103a): Python binding of ``libfp8gemm.so``.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams.  The C ABI is declared in ``include/fp8gemm.h``;
+functions here carry the same names and take torch tensors:
+
+    fp8_quantize_1x128(x, q, sA)                      x bf16 [M,K] -> q e4m3 [M,K], sA f32 [K/128, ld_sa]
+    fp8_quantize_128x128(w, q, sB)                    w bf16 [E,N,K] (or [N,K]) -> q, sB f32 [E,ceil(N/128),K/128]
+    fp8_gemm_nt(A, sA, B, sB, D)                      D bf16 [M,N] = A [M,K] x B [N,K]^T with block scales
+    fp8_grouped_gemm_contiguous(A, sA, B, sB, D, group_offsets)
+    fp8_grouped_gemm_masked(A, sA, B, sB, D, masked_m)
+
+e4m3 tensors may be torch.uint8 or torch.float8_e4m3fn.  Work is enqueued on the
+current CUDA stream of the tensors' device.  A non-zero status raises Fp8GemmError.
+Convenience wrappers (``quantize_1x128``, ``quantize_128x128``, ``gemm_nt``) allocate
+their outputs with torch and call the above.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libfp8gemm.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "fp8gemm.h")
+
+STATUS = {
+    0: "FP8G_OK", 1: "FP8G_ERR_INVALID_ARG", 2: "FP8G_ERR_ALIGNMENT",
+    3: "FP8G_ERR_UNSUPPORTED_DEVICE", 4: "FP8G_ERR_CUDA", 5: "FP8G_ERR_TIMEOUT",
+    6: "FP8G_ERR_DEVICE_ASSERT",
+}
+
+
+class Fp8GemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what} failed: {STATUS.get(code, code)}")
+
+
+_lib = None
+
+_I64, _I32, _P, _FP = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
+_SIGNATURES = {
+    "fp8_quantize_1x128": [_P, _I64, _I64, _I64, _P, _I64, _FP, _I64, _P],
+    "fp8_quantize_128x128": [_P, _I64, _I64, _I64, _P, _FP, _P],
+    "fp8_gemm_nt": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_contiguous": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_masked": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8g_get_status": [_P],
+    "fp8g_last_config": [ctypes.POINTER(ctypes.c_int)] * 3,
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built (there is no fallback path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m moe_grouped_gemm_block_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        handle.fp8g_status_string.argtypes = [ctypes.c_int]
+        handle.fp8g_status_string.restype = ctypes.c_char_p
+        _lib = handle
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/fp8gemm.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return re.findall(r"^(?:int|const char\*)\s+(\w+)\(", text, flags=re.M)
+
+
+def status_string(code: int) -> str:
+    return lib().fp8g_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise Fp8GemmError(code, what)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def _is_fp8(t: torch.Tensor) -> bool:
+    return t.dtype in (torch.uint8, torch.float8_e4m3fn)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+# ------------------------------------------------------------------ C-ABI calls
+
+def fp8_quantize_1x128(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor) -> None:
+    _need(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1, "x: bf16 [M,K], K contiguous")
+    _need(_is_fp8(q) and q.shape == x.shape and q.stride(1) == 1, "q: e4m3 [M,K]")
+    M, K = x.shape
+    _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1,
+          "sA: f32 [K/128, ld_sa]")
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_quantize_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(sA), ld_sa,
+                                    _stream(x)), "fp8_quantize_1x128")
+
+
+def fp8_quantize_128x128(w: torch.Tensor, q: torch.Tensor, sB: torch.Tensor) -> None:
+    _need(w.dtype == torch.bfloat16 and w.is_contiguous() and w.dim() in (2, 3), "w: bf16 [E,N,K] contiguous")
+    _need(_is_fp8(q) and q.shape == w.shape and q.is_contiguous(), "q: e4m3, same shape as w")
+    E, N, K = (1, *w.shape) if w.dim() == 2 else w.shape
+    _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() == E * ((N + 127) // 128) * (K // 128),
+          "sB: f32 [E, ceil(N/128), K/128] contiguous")
+    _check(lib().fp8_quantize_128x128(_ptr(w), E, N, K, _ptr(q), _ptr(sB), _stream(w)),
+           "fp8_quantize_128x128")
+
+
+def fp8_gemm_nt(A, sA, B, sB, D) -> None:
+    _need(_is_fp8(A) and A.dim() == 2 and A.stride(1) == 1, "A: e4m3 [M,K]")
+    _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
+    _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
+    _need(sA.dtype == torch.float32 and sB.dtype == torch.float32 and sB.is_contiguous(), "scales: f32")
+    M, K = A.shape
+    N = B.shape[0]
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_gemm_nt(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
+                             _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt")
+
+
+def fp8_grouped_gemm_contiguous(A, sA, B, sB, D, group_offsets) -> None:
+    _need(_is_fp8(A) and A.dim() == 2 and A.is_contiguous(), "A: e4m3 [M_total,K] contiguous")
+    _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
+    _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [M_total,N] contiguous")
+    _need(group_offsets.dtype == torch.int32 and group_offsets.is_cuda, "group_offsets: int32 device tensor")
+    M_total, K = A.shape
+    E, N, _ = B.shape
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_grouped_gemm_contiguous(_ptr(A), _ptr(sA), ld_sa, _ptr(B), _ptr(sB), _ptr(D),
+                                             _ptr(group_offsets), E, M_total, N, K, _stream(A)),
+           "fp8_grouped_gemm_contiguous")
+
+
+def fp8_grouped_gemm_masked(A, sA, B, sB, D, masked_m) -> None:
+    _need(_is_fp8(A) and A.dim() == 3 and A.is_contiguous(), "A: e4m3 [E,cap,K] contiguous")
+    _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
+    _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [E,cap,N] contiguous")
+    _need(masked_m.dtype == torch.int32 and masked_m.is_cuda, "masked_m: int32 device tensor")
+    E, cap, K = A.shape
+    N = B.shape[1]
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_grouped_gemm_masked(_ptr(A), _ptr(sA), ld_sa, _ptr(B), _ptr(sB), _ptr(D),
+                                         _ptr(masked_m), E, cap, N, K, _stream(A)),
+           "fp8_grouped_gemm_masked")
+
+
+def fp8g_get_status(stream: torch.cuda.Stream | None = None) -> int:
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    return lib().fp8g_get_status(s)
+
+
+def fp8g_last_config() -> dict:
+    bn, st, gr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().fp8g_last_config(ctypes.byref(bn), ctypes.byref(st), ctypes.byref(gr)), "fp8g_last_config")
+    return {"block_n": bn.value, "stages": st.value, "grid": gr.value}
+
+
+# ------------------------------------------------------------------ allocating wrappers
+
+def round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+def quantize_1x128(x: torch.Tensor, ld_sa: int | None = None):
+    """bf16 [M,K] -> (q uint8 [M,K], sA f32 [K/128, ld_sa]); ld_sa defaults to round_up(M, 4)."""
+    M, K = x.shape
+    ld = ld_sa or max(round_up(M, 4), 4)
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sA = torch.zeros((K // 128, ld), dtype=torch.float32, device=x.device)
+    fp8_quantize_1x128(x, q, sA)
+    return q, sA
+
+
+def quantize_128x128(w: torch.Tensor):
+    """bf16 [N,K] or [E,N,K] -> (q uint8, sB f32 [(E,) ceil(N/128), K/128])."""
+    N, K = w.shape[-2:]
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sB = torch.empty((*w.shape[:-2], (N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8_quantize_128x128(w, q, sB)
+    return q, sB
+
+
+def gemm_nt(A, sA, B, sB) -> torch.Tensor:
+    D = torch.empty((A.shape[0], B.shape[0]), dtype=torch.bfloat16, device=A.device)
+    fp8_gemm_nt(A, sA, B, sB, D)
+    return D

@@ -1,0 +1,634 @@
+// gemm.cu -- FP8 e4m3 block-scaled GEMM for sm_103a: dense NT, contiguous-grouped and
+// masked-grouped MoE forms, one persistent warp-specialised kernel template.
+//
+// What is computed ("DeepGEMM FP8 walk-through" sec. 2.2-2.3, "DeepGEMM explainer"
+// sec. 3.1-3.3): D = bf16( sum_kb P_kb * sA[kb][m] * sB[n/128][kb] ), P_kb the e4m3 x e4m3
+// product of one 128-wide K block, accumulated in FP32.  The scales are applied inside the
+// GEMM pipeline, not by a separate dequantisation pass.
+//
+// GB300 design (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0        TMA producer: A tile (128 x 128 B), B tile (BN x 128 B), the 128 A-row
+//                 scales of the K block -> one stage of a STAGES-deep shared-memory ring,
+//                 signalled through a full/empty mbarrier pair per stage.
+//   warp 1        allocates TMEM; one lane issues 4 tcgen05.mma kind::f8f6f4 (K = 32 each)
+//                 per K block into a FRESH TMEM partial (the first MMA does not accumulate),
+//                 double-buffered (2 x BN columns) so the MMA of block kb+1 overlaps the
+//                 promotion of block kb.
+//   warps 2..     promotion + epilogue: tcgen05.ld the partial, acc = fma(P, sa*sb, acc) in
+//                 FP32 registers (one TMEM lane = one output row per thread), then after the
+//                 last K block convert to BF16 and store through shared memory with TMA
+//                 (64-byte-swizzled 32 x 32 boxes).  Rows past a masked expert's count are
+//                 never written.
+// Every wait is bounded: a wait that runs past its cycle budget records FP8G_ERR_TIMEOUT in
+// the status word, raises a shared abort flag, and every role returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdlib>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8g {
+namespace {
+
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+
+constexpr int BM = 128;  // rows per tile = TMEM lanes
+constexpr int BK = 128;  // K per stage = the scaling block
+constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a band)
+
+template <int BN>
+struct Cfg {
+  static constexpr int kEpiCols = BN >= 128 ? 128 : BN;  // columns per epilogue warp
+  static constexpr int kEpiGroups = BN / kEpiCols;       // warpgroups of epilogue warps
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
+  // BN = 256: three full warpgroups (producer / MMA / 2 idle, then 2 epilogue warpgroups) so
+  // that setmaxnreg can move registers to the epilogue: the launch gives 384 x 168 = 64512,
+  // rebalanced to 128 x 40 + 256 x 232 = 64512.  Otherwise: 2 warps + 1 epilogue warpgroup.
+  static constexpr int kEpiWarp0 = BN == 256 ? 4 : 2;
+  static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
+  static constexpr bool kRebalance = BN == 256;
+  static constexpr uint32_t kRegsLow = 40, kRegsHigh = 232;
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr uint32_t kABytes = BM * BK;
+  static constexpr uint32_t kBBytes = BN * BK;
+  static constexpr uint32_t kSABytes = BM * 4;
+  static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per warp
+  // shared-memory carve-up (offsets from a 1024-aligned base)
+  static constexpr uint32_t kOffA = 0;
+  static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+  static constexpr uint32_t kOffOut = kOffB + kStages * kBBytes;
+  static constexpr uint32_t kOffSA = kOffOut + kEpiWarps * kOutBytes;
+  static constexpr uint32_t kOffBar = kOffSA + kStages * kSABytes;
+  static constexpr uint32_t kNumBars = 2 * kStages + 4;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffTable = kOffMisc + 16;
+  static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
+  static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+};
+
+struct GemmArgs {
+  int32_t rows;      // rows of A / D (M, M_total or E*cap)
+  int32_t N, KB, NBs, E, cap;
+  int32_t num_m;     // m-blocks (dense / contiguous)
+  int32_t num_n;     // n-blocks of BN
+  int32_t num_tiles; // dense / contiguous tile count
+  const float* sB;
+  __nv_bfloat16* D;
+  int64_t ldd;
+  const int32_t* groups;  // contiguous: offsets [E+1]; masked: counts [E]
+  unsigned int* status;
+  long long budget;
+};
+
+struct Tile {
+  int32_t a_row;  // first row of A / D (and the x coordinate into the scale map)
+  int32_t n0;     // first column
+  int32_t g;      // expert
+  int32_t rows;   // rows of the tile that may be stored (masked tail), else BM
+};
+
+// Tile index -> tile.  Returns false when the tile has no rows to compute.
+template <int BN, int MODE>
+__device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table, int32_t t,
+                                         Tile& ti) {
+  if (MODE == kMasked) {
+    // table[e] = sum of m-blocks of experts < e; an expert's tiles are (nb, mb), mb fastest
+    int lo = 0, hi = a.E;  // find e with table[e]*num_n <= t < table[e+1]*num_n
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int64_t>(table[mid]) * a.num_n <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int32_t mbs = table[e + 1] - table[e];
+    if (mbs <= 0) return false;
+    const int32_t local = t - table[e] * a.num_n;
+    const int32_t mb = local % mbs, nb = local / mbs;
+    int32_t cnt = __ldg(a.groups + e);
+    cnt = min(max(cnt, 0), a.cap);
+    ti.g = e;
+    ti.a_row = e * a.cap + mb * BM;
+    ti.n0 = nb * BN;
+    ti.rows = min(BM, cnt - mb * BM);
+    return ti.rows > 0;
+  } else {
+    const int32_t band_tiles = kBandM * a.num_n;
+    const int32_t band = t / band_tiles, r = t - band * band_tiles;
+    const int32_t m_first = band * kBandM;
+    const int32_t gm = min(kBandM, a.num_m - m_first);
+    const int32_t mb = m_first + r % gm, nb = r / gm;
+    ti.a_row = mb * BM;
+    ti.n0 = nb * BN;
+    ti.rows = min(BM, a.rows - ti.a_row);  // rows past the matrix edge are not stored
+    ti.g = 0;
+    if (MODE == kContiguous) {
+      // expert e with offsets[e] <= row < offsets[e+1]: first index with offsets[i] > row, minus 1
+      int lo = 0, hi = a.E + 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (table[mid] > ti.a_row) hi = mid; else lo = mid + 1;
+      }
+      const int e = lo - 1;
+      if (e < 0 || e >= a.E) return false;
+      ti.g = e;
+    }
+    return true;
+  }
+}
+
+// Bounded wait on an mbarrier phase.  On timeout: flag the CTA, record the status.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmArgs& a,
+                                             volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > a.budget) {
+      *abort_flag = 1;
+      record_status(a.status, FP8G_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
+                    const GemmArgs a) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = smem_u32(smem);
+  if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) record_status(a.status, FP8G_ERR_DEVICE_ASSERT);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* sSA = reinterpret_cast<float*>(smem + C::kOffSA);
+  const uint32_t bar0 = base + C::kOffBar;
+  auto full = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty = [&](uint32_t s) { return bar0 + 8u * (S + s); };
+  auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 + b); };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);  // [0] tmem base, [1] abort
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  int32_t* table = reinterpret_cast<int32_t*>(smem + C::kOffTable);
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1 + C::kEpiWarps);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), C::kEpiWarps);
+    }
+    misc[1] = 0;
+    misc[2] = 0;  // set when the group table is out of contract
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    prefetch_tmap(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc(base + C::kOffMisc, C::kTmemCols);
+    tmem_relinquish();
+  }
+  // Group tables (grouped modes), built by the first epilogue warp.
+  if (MODE == kContiguous && warp == C::kEpiWarp0) {
+    bool bad = false;
+    for (int i = lane; i <= a.E; i += 32) {
+      const int32_t v = __ldg(a.groups + i);
+      table[i] = v;
+      if (v < 0 || (v & (BM - 1)) || v > a.rows) bad = true;
+      if (i < a.E && __ldg(a.groups + i + 1) < v) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+      misc[2] = 1;
+      record_status(a.status, FP8G_ERR_DEVICE_ASSERT);
+    }
+  }
+  if (MODE == kMasked && warp == C::kEpiWarp0) {
+    int32_t running = 0;
+    bool bad = false;
+    if (lane == 0) table[0] = 0;
+    for (int e0 = 0; e0 < a.E; e0 += 32) {
+      const int e = e0 + lane;
+      int32_t mbs = 0;
+      if (e < a.E) {
+        const int32_t cnt = __ldg(a.groups + e);
+        if (cnt < 0 || cnt > a.cap) bad = true;
+        const int32_t c = min(max(cnt, 0), a.cap);
+        mbs = (c + BM - 1) / BM;
+      }
+      int32_t incl = mbs;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (e < a.E) table[e + 1] = running + incl;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(a.status, FP8G_ERR_DEVICE_ASSERT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+
+  int32_t num_tiles = a.num_tiles;
+  if (MODE == kMasked) num_tiles = table[a.E] * a.num_n;
+  if (MODE == kContiguous && misc[2]) num_tiles = 0;
+  if (warp < C::kEpiWarp0) {
+    if constexpr (C::kRebalance) regs_release<C::kRegsLow>();
+    if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        Tile ti;
+        if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
+        for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1u;
+          if (!wait_bounded(empty(s), ph ^ 1u, a, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes + C::kSABytes);
+          tma_load_2d(base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
+          tma_load_3d(base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
+          tma_load_2d(base + C::kOffSA + s * C::kSABytes, &tmSA, full(s), ti.a_row, kb);
+        }
+      }
+      if (!ok) {  // let the loads already issued land before the CTA exits
+        const uint32_t n = it < S ? it : S;
+        for (uint32_t i = it - n; i < it; ++i) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(full(i % S), (i / S) & 1u) && clock64() - t0 < a.budget) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        Tile ti;
+        if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
+        for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1u;
+          const uint32_t b = it & 1u, tph = (it >> 1) & 1u;
+          if (!wait_bounded(tempty(b), tph ^ 1u, a, abort_flag)) { ok = false; break; }
+          if (!wait_bounded(full(s), ph, a, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = base + C::kOffA + s * C::kABytes;
+          const uint32_t b_addr = base + C::kOffB + s * C::kBBytes;
+          const uint32_t d_tmem = tmem_base + b * BN;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            mma_f8f6f4(d_tmem, smem_desc_k_sw128(a_addr + 32 * k), smem_desc_k_sw128(b_addr + 32 * k),
+                       idesc, k > 0 ? 1u : 0u);
+          }
+          mma_commit(empty(s));
+          mma_commit(tfull(b));
+        }
+      }
+      if (!ok && it > 0) {  // wait for the MMAs already issued before TMEM is released
+        const uint32_t last = it - 1;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(tfull(last & 1u), (last >> 1) & 1u) && clock64() - t0 < a.budget) {
+        }
+      }
+    }
+  }
+  } else {
+    if constexpr (C::kRebalance) regs_acquire<C::kRegsHigh>();
+    // ------------------------------------------------------------ promotion + epilogue
+    const int ew = warp - C::kEpiWarp0;  // epilogue warp index
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int col0 = (ew >> 2) * C::kEpiCols;  // column offset of this warp inside the tile
+    const int row = q * 32 + lane;       // tile row owned by this thread
+    const uint32_t out_addr = base + C::kOffOut + ew * C::kOutBytes;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      Tile ti;
+      if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
+      const int32_t ncol0 = ti.n0 + col0;
+      const bool has_cols = ncol0 < a.N;
+      const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
+      float acc[C::kEpiCols];
+#pragma unroll
+      for (int j = 0; j < C::kEpiCols; ++j) acc[j] = 0.0f;
+      float sb_next = has_cols ? ld_nc_f32(sbp) : 0.0f;
+      for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
+        const uint32_t s = it % S, ph = (it / S) & 1u;
+        const uint32_t b = it & 1u, tph = (it >> 1) & 1u;
+        const float sb_cur = sb_next;
+        if (has_cols && kb + 1 < a.KB) sb_next = ld_nc_f32(sbp + kb + 1);
+        if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
+        const float scale = sSA[s * BM + row] * sb_cur;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
+        if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
+#pragma unroll
+        for (int c = 0; c < C::kEpiCols / 32; ++c) {
+          float v[32];
+          tmem_ld32_sync(taddr + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(v[j], scale, acc[c * 32 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(b));
+      }
+      if (!ok) break;
+      // ---- epilogue: this warp holds rows q*32 .. q*32+31, columns ncol0 .. ncol0+kEpiCols-1
+      const int nvalid = min(32, ti.rows - q * 32);
+      if (nvalid <= 0 || !has_cols) continue;
+      if (MODE != kMasked || nvalid == 32) {
+#pragma unroll
+        for (int j = 0; j < C::kEpiCols / 32; ++j) {
+          if (ncol0 + 32 * j >= a.N) break;
+          if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
+          __syncwarp();
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(acc[32 * j + 2 * i], acc[32 * j + 2 * i + 1]);
+          const uint32_t rowaddr = out_addr + lane * 64;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            // 64-byte swizzle: 16-byte chunk index XOR address bits 7-8 (= row / 2 mod 4)
+            st_shared_v4(rowaddr + ((ch ^ ((lane >> 1) & 3)) << 4), p[4 * ch], p[4 * ch + 1],
+                         p[4 * ch + 2], p[4 * ch + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, out_addr, ncol0 + 32 * j, ti.a_row + q * 32);
+            bulk_commit();
+          }
+        }
+      } else if (lane < nvalid) {
+        // partial rows of a masked expert: plain stores, row by row
+        __nv_bfloat16* drow = a.D + static_cast<int64_t>(ti.a_row + q * 32 + lane) * a.ldd + ncol0;
+#pragma unroll
+        for (int j = 0; j < C::kEpiCols / 8; ++j) {
+          if (ncol0 + 8 * j < a.N) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+            v.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+            v.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+            v.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+            *reinterpret_cast<uint4*>(drow + 8 * j) = v;
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int BN>
+constexpr uint32_t smem_bytes(int table_entries) {
+  return Cfg<BN>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
+}
+
+constexpr int kMaxExperts = 4096;
+
+template <int BN, int MODE>
+int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
+                  const CUtensorMap& tSA, const CUtensorMap& tD, int grid, int table_entries,
+                  cudaStream_t stream) {
+  auto kern = fp8_gemm_kernel<BN, MODE>;
+  static std::atomic<uint64_t> attr_set{0};  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN>(kMaxExperts + 1))) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8G_ERR_CUDA;
+    }
+    if constexpr (Cfg<BN>::kRebalance) {
+      // setmaxnreg.inc waits until the registers it asks for are free: the launch must hold
+      // at least what the rebalanced warpgroups use, or the epilogue would never start.
+      cudaFuncAttributes fa{};
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8G_ERR_CUDA;
+      }
+      if (fa.numRegs * Cfg<BN>::kThreads < 128 * static_cast<int>(Cfg<BN>::kRegsLow) +
+                                               256 * static_cast<int>(Cfg<BN>::kRegsHigh))
+        return FP8G_ERR_CUDA;
+    }
+    attr_set.fetch_or(bit);
+  }
+  kern<<<grid, Cfg<BN>::kThreads, smem_bytes<BN>(table_entries), stream>>>(tA, tB, tSA, tD, args);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0;
+
+// FP8G_BLOCK_N (64, 128 or 256) forces the tile width; read on every call.
+int env_block_n() {
+  const char* e = std::getenv("FP8G_BLOCK_N");
+  const int x = e ? std::atoi(e) : 0;
+  return (x == 64 || x == 128 || x == 256) ? x : 0;
+}
+
+// Pick BN: fewest (waves x per-tile cost), the per-tile cost growing with BN plus a fixed
+// promotion/epilogue overhead.  Small-M shapes get narrow tiles so that every SM streams B.
+int choose_block_n(int64_t m_blocks, int64_t N, int sms) {
+  if (int v = env_block_n()) return v;
+  int best = 256;
+  double best_cost = 1e300;
+  for (int bn : {256, 128, 64}) {
+    const int64_t tiles = m_blocks * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (bn + 64);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+struct Operands {
+  const void* A;
+  int64_t lda;
+  const float* sA;
+  int64_t ld_sa;
+  const void* B;
+  int64_t ldb;
+  const float* sB;
+  void* D;
+  int64_t ldd;
+  int64_t rows, N, K, E, cap;
+  const int32_t* groups;
+};
+
+template <int MODE>
+int run_gemm(const Operands& o, cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  if (o.rows == 0) return FP8G_OK;
+
+  const int64_t m_blocks = (MODE == kMasked) ? o.E * ((o.cap + BM - 1) / BM) : (o.rows + BM - 1) / BM;
+  const int bn = choose_block_n(m_blocks, o.N, dev->sm_count);
+
+  GemmArgs a{};
+  a.rows = static_cast<int32_t>(o.rows);
+  a.N = static_cast<int32_t>(o.N);
+  a.KB = static_cast<int32_t>(o.K / BK);
+  a.NBs = static_cast<int32_t>((o.N + 127) / 128);
+  a.E = static_cast<int32_t>(o.E);
+  a.cap = static_cast<int32_t>(o.cap);
+  a.num_m = static_cast<int32_t>((o.rows + BM - 1) / BM);
+  a.num_n = static_cast<int32_t>((o.N + bn - 1) / bn);
+  a.num_tiles = a.num_m * a.num_n;
+  a.sB = o.sB;
+  a.D = static_cast<__nv_bfloat16*>(o.D);
+  a.ldd = o.ldd;
+  a.groups = o.groups;
+  a.status = dev->status;
+  a.budget = wait_budget_cycles();
+
+  CUtensorMap tA, tB, tSA, tD;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(o.K), static_cast<uint64_t>(o.rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(o.lda)};
+    const uint32_t box[2] = {BK, BM};
+    if ((st = encode_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, o.A, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
+      return st;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(o.K), static_cast<uint64_t>(o.N),
+                              static_cast<uint64_t>(o.E)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(o.ldb), static_cast<uint64_t>(o.ldb * o.N)};
+    const uint32_t box[3] = {BK, static_cast<uint32_t>(bn), 1};
+    if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, o.B, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
+      return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(o.rows), static_cast<uint64_t>(o.K / BK)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(o.ld_sa * 4)};
+    const uint32_t box[2] = {BM, 1};
+    if ((st = encode_tmap(&tSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, o.sA, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != FP8G_OK)
+      return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.rows)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(o.ldd * 2)};
+    const uint32_t box[2] = {32, 32};
+    if ((st = encode_tmap(&tD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.D, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_64B)) != FP8G_OK)
+      return st;
+  }
+
+  int64_t tiles_upper = (MODE == kMasked) ? m_blocks * a.num_n : static_cast<int64_t>(a.num_tiles);
+  int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(tiles_upper, 1), dev->sm_count));
+  const int table_entries = (MODE == kDense) ? 0 : static_cast<int>(o.E + 1);
+
+  t_last_bn = bn;
+  t_last_grid = grid;
+  switch (bn) {
+    case 256:
+      t_last_stages = Cfg<256>::kStages;
+      return launch_kernel<256, MODE>(a, tA, tB, tSA, tD, grid, table_entries, stream);
+    case 128:
+      t_last_stages = Cfg<128>::kStages;
+      return launch_kernel<128, MODE>(a, tA, tB, tSA, tD, grid, table_entries, stream);
+    default:
+      t_last_stages = Cfg<64>::kStages;
+      return launch_kernel<64, MODE>(a, tA, tB, tSA, tD, grid, table_entries, stream);
+  }
+}
+
+constexpr int64_t kMaxI32 = 0x7FFFFFFF;
+
+}  // namespace
+}  // namespace fp8g
+
+using namespace fp8g;
+
+extern "C" int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa,
+                           const void* B, int64_t ldb, const float* sB, void* D, int64_t ldd,
+                           int64_t M, int64_t N, int64_t K, void* stream) {
+  if (!A || !sA || !B || !sB || !D) return FP8G_ERR_INVALID_ARG;
+  if (M < 0 || M > kMaxI32 || N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 ||
+      K > kMaxI32)
+    return FP8G_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldd < N || ld_sa < M) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0 || ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr};
+  return run_gemm<kDense>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_contiguous(const void* A, const float* sA, int64_t ld_sa,
+                                           const void* B, const float* sB, void* D,
+                                           const int32_t* group_offsets, int32_t E,
+                                           int64_t M_total, int64_t N, int64_t K, void* stream) {
+  if (!A || !sA || !B || !sB || !D || !group_offsets) return FP8G_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts || M_total < 0 || M_total > kMaxI32 || M_total % 128 != 0 ||
+      N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32 ||
+      ld_sa < M_total || N * E > kMaxI32 * 64)
+    return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      (reinterpret_cast<uintptr_t>(group_offsets) & 3u) || ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, K, sA, ld_sa, B, K, sB, D, N, M_total, N, K, E, 0, group_offsets};
+  return run_gemm<kContiguous>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t ld_sa,
+                                       const void* B, const float* sB, void* D,
+                                       const int32_t* masked_m, int32_t E, int64_t cap, int64_t N,
+                                       int64_t K, void* stream) {
+  if (!A || !sA || !B || !sB || !D || !masked_m) return FP8G_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts || cap < 0 || cap % 16 != 0 || static_cast<int64_t>(E) * cap > kMaxI32 ||
+      N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32 ||
+      ld_sa < static_cast<int64_t>(E) * cap)
+    return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      (reinterpret_cast<uintptr_t>(masked_m) & 3u) || ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, K, sA, ld_sa, B, K, sB, D, N, static_cast<int64_t>(E) * cap, N, K, E, cap, masked_m};
+  return run_gemm<kMasked>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8g_last_config(int* block_n, int* stages, int* grid) {
+  if (!block_n || !stages || !grid) return FP8G_ERR_INVALID_ARG;
+  *block_n = t_last_bn;
+  *stages = t_last_stages;
+  *grid = t_last_grid;
+  return FP8G_OK;
+}

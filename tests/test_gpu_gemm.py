@@ -1,0 +1,318 @@
+"""GPU parity of the block-scaled GEMMs (dense, contiguous-grouped, masked-grouped)
+against the oracle, through the C ABI.
+
+Small shapes are compared in full (several tiles, ragged tails, every tile width);
+the full-size workloads are compared on sampled rows x sampled 128-column blocks,
+after checking that the GPU-quantised operands equal the oracle's bytes there, so the
+oracle never takes an input from the CUDA path.  Rows a grouped call must not write
+are checked bit for bit against a sentinel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_block_gb300 as g
+from moe_grouped_gemm_block_gb300.workloads import WORKLOADS, make_inputs, round_up
+from oracle import gemm_nt, grouped_contiguous, grouped_masked, quantize_128x128, quantize_1x128
+from tests.gpu_util import (assert_gemm_close, bf16_bits, bf16_to_np, block_n, check_status, need_gpu,
+                            sa_from_device, sa_to_device, u8)
+
+pytestmark = pytest.mark.gpu
+SENTINEL = 0x7FC1  # a bf16 NaN pattern the GEMM never produces
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    need_gpu()
+
+
+def _draw(shape, seed, std=1.0):
+    gen = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=gen) * std).to(torch.bfloat16).float().numpy()
+
+
+def _problem(M, N, K, seed):
+    x = _draw((M, K), seed, 2.0)
+    if K >= 256:
+        x[:, 3] *= 50  # an outlier channel
+    qa, sa = quantize_1x128(x)
+    qb, sb = quantize_128x128(_draw((N, K), seed + 1, 1 / np.sqrt(K)))
+    return qa, sa, qb, sb
+
+
+def _dense_gpu(qa, sa, qb, sb, bn=None):
+    M, K = qa.shape
+    N = qb.shape[0]
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with block_n(bn):
+        g.fp8_gemm_nt(u8(qa), sa_to_device(sa), u8(qb), torch.from_numpy(sb).cuda(), D)
+    torch.cuda.synchronize()
+    check_status()
+    return D
+
+
+@pytest.mark.parametrize("M,N,K,bn", [
+    (128, 256, 512, None), (1, 16, 128, 64), (64, 64, 128, None), (200, 208, 384, 256),
+    (200, 208, 384, 128), (200, 208, 384, 64), (300, 512, 1024, 256), (129, 272, 256, 128),
+    (64, 1792, 7168, 64), (257, 1024, 640, 256), (513, 384, 256, None),
+])
+def test_dense_small_shapes(M, N, K, bn):
+    qa, sa, qb, sb = _problem(M, N, K, seed=M * 7 + N + K)
+    D = _dense_gpu(qa, sa, qb, sb, bn)
+    assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} bn={bn}")
+
+
+def test_dense_strided_operands():
+    M, N, K = 150, 160, 384
+    qa, sa, qb, sb = _problem(M, N, K, seed=3)
+    A = torch.zeros((M, K + 64), dtype=torch.uint8, device="cuda")
+    A[:, :K] = u8(qa)
+    B = torch.zeros((N, K + 128), dtype=torch.uint8, device="cuda")
+    B[:, :K] = u8(qb)
+    D = torch.full((M, N + 24), 7.0, dtype=torch.bfloat16, device="cuda")
+    g.fp8_gemm_nt(A[:, :K], sa_to_device(sa, ld_sa=160), B[:, :K], torch.from_numpy(sb).cuda(), D[:, :N])
+    torch.cuda.synchronize()
+    check_status()
+    assert_gemm_close(bf16_to_np(D[:, :N]), gemm_nt(qa, sa, qb, sb), "strided")
+    assert torch.all(D[:, N:] == 7.0)
+
+
+def test_dense_tiny_workload_in_full():
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, "cpu")
+    qa, sa = quantize_1x128(inp["A"].float().numpy())
+    qb, sb = quantize_128x128(inp["B"].float().numpy())
+    D = _dense_gpu(qa, sa, qb, sb)
+    assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), "tiny")
+
+
+def test_dense_all_scales_equal_power_of_two_case():
+    # per-tensor special case: scaling A by 2^k and its scales by 2^-k must not change D
+    qa, sa, qb, sb = _problem(256, 512, 512, seed=11)
+    D1 = _dense_gpu(qa, sa, qb, sb)
+    D2 = _dense_gpu(qa, sa * np.float32(2.0 ** 10), qb, sb * np.float32(2.0 ** -10))
+    assert torch.equal(D1, D2)
+
+
+def _check_weights_equal(qB_gpu, sB_gpu, B_bf16, nblocks, e=None):
+    """GPU-quantised weight rows of the given 128-row blocks == oracle bytes; returns them."""
+    qs, ss, cols = [], [], []
+    for nb in nblocks:
+        rows = slice(nb * 128, (nb + 1) * 128)
+        src = B_bf16[rows] if e is None else B_bf16[e, rows]
+        q_ref, s_ref = quantize_128x128(src.float().cpu().numpy())
+        got_q = (qB_gpu[rows] if e is None else qB_gpu[e, rows]).cpu().numpy()
+        got_s = (sB_gpu[nb] if e is None else sB_gpu[e, nb]).cpu().numpy()
+        assert np.array_equal(got_q, q_ref) and np.array_equal(got_s, s_ref[0])
+        qs.append(q_ref)
+        ss.append(s_ref)
+        cols.append(np.arange(nb * 128, nb * 128 + q_ref.shape[0]))
+    return np.concatenate(qs), np.concatenate(ss), np.concatenate(cols)
+
+
+def _check_acts_equal(qA_gpu, sA_gpu, A_bf16, rows):
+    q_ref, s_ref = quantize_1x128(A_bf16[rows].float().cpu().numpy())
+    M = A_bf16.shape[0]
+    assert np.array_equal(qA_gpu[rows].cpu().numpy(), q_ref)
+    assert np.array_equal(sa_from_device(sA_gpu, M)[rows], s_ref)
+    return q_ref, s_ref
+
+
+@pytest.mark.parametrize("name", ["decode", "large_4096", "large_4096x8192"])
+def test_dense_full_size_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, "cuda")
+    A, B = inp["A"], inp["B"]
+    qA, sA = g.quantize_1x128(A)
+    qB, sB = g.quantize_128x128(B)
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    g.fp8_gemm_nt(qA, sA, qB, sB, D)
+    torch.cuda.synchronize()
+    check_status()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([rng.choice(w.M, min(w.M, 48), replace=False), [w.M - 1]]))
+    nbs = sorted({0, (w.N - 1) // 128, int(rng.integers(w.N // 128))})
+    qa, sa = _check_acts_equal(qA, sA, A, rows)
+    qb, sb_rows, cols = _check_weights_equal(qB, sB, B, nbs)
+    ref = gemm_nt(qa, sa, qb, np.concatenate([s for s in sb_rows.reshape(len(nbs), 1, -1)]),
+                  n_index=np.repeat(np.arange(len(nbs)), 128) * 128)
+    got = bf16_to_np(D[rows][:, cols])
+    assert_gemm_close(got, ref, name)
+    assert torch.isfinite(D.float()).all()
+
+
+# ---------------------------------------------------------------- contiguous
+
+def _contig_problem(sizes, N, K, seed, extra_rows=0):
+    E = len(sizes)
+    offs = [0]
+    for s in sizes:
+        offs.append(offs[-1] + round_up(s, 128))
+    M_total = offs[-1] + extra_rows
+    x = np.zeros((M_total, K), np.float32)
+    for e, s in enumerate(sizes):
+        x[offs[e]:offs[e] + s] = _draw((s, K), seed + e, 1.5)
+    qa, sa = quantize_1x128(x)
+    qbs, sbs = zip(*(quantize_128x128(_draw((N, K), seed + 100 + e, 1 / np.sqrt(K))) for e in range(E)))
+    return qa, sa, np.stack(qbs), np.stack(sbs), np.array(offs, np.int32)
+
+
+def _contig_gpu(qa, sa, qb, sb, offs, bn=None):
+    M_total, K = qa.shape
+    N = qb.shape[1]
+    D = torch.full((M_total, N), 0, dtype=torch.int16, device="cuda").fill_(SENTINEL).view(torch.bfloat16)
+    with block_n(bn):
+        g.fp8_grouped_gemm_contiguous(u8(qa), sa_to_device(sa), u8(qb), torch.from_numpy(sb).cuda(), D,
+                                      torch.from_numpy(offs).cuda())
+    torch.cuda.synchronize()
+    return D
+
+
+@pytest.mark.parametrize("bn", [None, 256, 128, 64])
+def test_contiguous_small(bn):
+    qa, sa, qb, sb, offs = _contig_problem([100, 0, 300, 128, 1], N=272, K=384, seed=5, extra_rows=128)
+    D = _contig_gpu(qa, sa, qb, sb, offs, bn)
+    check_status()
+    init = np.full((qa.shape[0], qb.shape[1]), SENTINEL, np.uint16)
+    ref = grouped_contiguous(qa, sa, qb, sb, offs, init)
+    got = bf16_bits(D)
+    last = offs[-1]
+    assert np.array_equal(got[last:], ref[last:])  # rows outside every group: untouched
+    assert_gemm_close(bf16_to_np(D[:last]), ref[:last], f"contiguous bn={bn}")
+
+
+def test_contiguous_pages_two_experts_eight_tokens():
+    qa, sa, qb, sb, offs = _contig_problem([8, 8], N=128, K=256, seed=9)
+    D = _contig_gpu(qa, sa, qb, sb, offs)
+    check_status()
+    ref = grouped_contiguous(qa, sa, qb, sb, offs, np.zeros((256, 128), np.uint16))
+    assert_gemm_close(bf16_to_np(D), ref, "2 experts x 8 tokens")
+    assert not bf16_to_np(D[8:128]).any() and not bf16_to_np(D[136:]).any()  # zero padding rows
+
+
+def test_contiguous_bad_offsets_sets_device_assert_and_writes_nothing():
+    qa, sa, qb, sb, offs = _contig_problem([128, 128], N=128, K=128, seed=2)
+    for bad in ([0, 100, 256], [0, 256, 128], [0, 128, 512]):
+        D = _contig_gpu(qa, sa, qb, sb, np.array(bad, np.int32))
+        assert g.fp8g_get_status() == 6
+        assert np.all(bf16_bits(D) == SENTINEL)
+    check_status()
+
+
+def test_contiguous_full_size_sampled():
+    w = WORKLOADS["moe_contiguous"]
+    inp = make_inputs(w, "cuda")
+    A, B, offs = inp["A"], inp["B"], inp["group_offsets"]
+    qA, sA = g.quantize_1x128(A)
+    qB, sB = g.quantize_128x128(B)
+    M_total = A.shape[0]
+    D = torch.empty((M_total, w.N), dtype=torch.bfloat16, device="cuda")
+    g.fp8_grouped_gemm_contiguous(qA, sA, qB, sB, D, offs.cuda())
+    torch.cuda.synchronize()
+    check_status()
+    rng = np.random.default_rng(3)
+    offs = offs.numpy()
+    for e in (0, 3, w.E - 1):
+        r0, r1 = int(offs[e]), int(offs[e + 1])
+        rows = np.unique(np.concatenate([rng.integers(r0, r1, 24), [r0, r1 - 1]]))
+        nbs = sorted({0, int(rng.integers(w.N // 128)), w.N // 128 - 1})
+        qa, sa = _check_acts_equal(qA, sA, A, rows)
+        qb, sb_rows, cols = _check_weights_equal(qB, sB, B, nbs, e=e)
+        ref = gemm_nt(qa, sa, qb, sb_rows.reshape(len(nbs), -1),
+                      n_index=np.repeat(np.arange(len(nbs)), 128) * 128)
+        assert_gemm_close(bf16_to_np(D[rows][:, cols]), ref, f"contiguous expert {e}")
+
+
+# ---------------------------------------------------------------- masked
+
+def _masked_gpu(qa, sa, qb, sb, masked, bn=None):
+    E, cap, K = qa.shape
+    N = qb.shape[1]
+    D = torch.full((E, cap, N), 0, dtype=torch.int16, device="cuda").fill_(SENTINEL).view(torch.bfloat16)
+    with block_n(bn):
+        g.fp8_grouped_gemm_masked(u8(qa), sa_to_device(sa.reshape(E * cap, -1)), u8(qb),
+                                  torch.from_numpy(sb).cuda(), D, torch.tensor(masked, dtype=torch.int32).cuda())
+    torch.cuda.synchronize()
+    return D
+
+
+def _masked_problem(E, cap, N, K, seed):
+    qa, sa = quantize_1x128(_draw((E * cap, K), seed, 1.5))
+    qbs, sbs = zip(*(quantize_128x128(_draw((N, K), seed + 50 + e, 1 / np.sqrt(K))) for e in range(E)))
+    return qa.reshape(E, cap, K), sa.reshape(E, cap, -1), np.stack(qbs), np.stack(sbs)
+
+
+@pytest.mark.parametrize("bn", [None, 256, 128, 64])
+def test_masked_small(bn):
+    E, cap, N, K = 5, 160, 272, 384
+    masked = [0, 1, 160, 37, 129]
+    qa, sa, qb, sb = _masked_problem(E, cap, N, K, seed=21)
+    D = _masked_gpu(qa, sa, qb, sb, masked, bn)
+    check_status()
+    ref = grouped_masked(qa, sa, qb, sb, masked, np.full((E, cap, N), SENTINEL, np.uint16))
+    got = bf16_bits(D)
+    for e in range(E):
+        m = masked[e]
+        assert np.all(got[e, m:] == SENTINEL), f"expert {e}: rows past masked_m written"
+        if m:
+            assert_gemm_close(bf16_to_np(D[e, :m]), ref[e, :m], f"masked e={e} bn={bn}")
+
+
+def test_masked_counts_out_of_range_are_clamped_and_flagged():
+    E, cap, N, K = 2, 32, 128, 128
+    qa, sa, qb, sb = _masked_problem(E, cap, N, K, seed=4)
+    D = _masked_gpu(qa, sa, qb, sb, [40, -3])
+    assert g.fp8g_get_status() == 6
+    ref = grouped_masked(qa, sa, qb, sb, [32, 0], np.full((E, cap, N), SENTINEL, np.uint16))
+    assert_gemm_close(bf16_to_np(D[0]), ref[0], "clamped")
+    assert np.all(bf16_bits(D[1]) == SENTINEL)
+
+
+def test_masked_full_size_sampled():
+    w = WORKLOADS["moe_masked"]
+    inp = make_inputs(w, "cuda")
+    A, B, masked = inp["A"], inp["B"], inp["masked_m"]
+    qA, sA = g.quantize_1x128(A.reshape(-1, w.K))
+    qB, sB = g.quantize_128x128(B)
+    D = torch.full((w.E, w.cap, w.N), 0, dtype=torch.int16, device="cuda").fill_(SENTINEL).view(torch.bfloat16)
+    g.fp8_grouped_gemm_masked(qA.view(w.E, w.cap, w.K), sA, qB, sB, D, masked.cuda())
+    torch.cuda.synchronize()
+    check_status()
+    bits = D.view(torch.int16)
+    for e in range(w.E):  # every row past the count is untouched, every valid row finite
+        m = int(masked[e])
+        assert bool((bits[e, m:] == SENTINEL).all()), e
+        assert bool(torch.isfinite(D[e, :m].float()).all()), e
+    rng = np.random.default_rng(4)
+    ms = masked.numpy()
+    picks = [int(np.argmax(ms)), int(np.argmin(np.where(ms > 0, ms, 10 ** 6))), 7]
+    for e in picks:
+        m = int(ms[e])
+        if m == 0:
+            continue
+        rows = np.unique(np.concatenate([rng.integers(0, m, 16), [0, m - 1]]))
+        nbs = sorted({0, int(rng.integers(w.N // 128)), w.N // 128 - 1})
+        flat = e * w.cap + rows
+        qa, sa = _check_acts_equal(qA, sA, A.reshape(-1, w.K), flat)
+        qb, sb_rows, cols = _check_weights_equal(qB, sB, B, nbs, e=e)
+        ref = gemm_nt(qa, sa, qb, sb_rows.reshape(len(nbs), -1),
+                      n_index=np.repeat(np.arange(len(nbs)), 128) * 128)
+        assert_gemm_close(bf16_to_np(D[e][rows][:, cols]), ref, f"masked expert {e}")
+
+
+def test_status_clear_after_many_calls_on_two_streams():
+    qa, sa, qb, sb = _problem(256, 512, 512, seed=8)
+    A, B, sBt = u8(qa), u8(qb), torch.from_numpy(sb).cuda()
+    sAt = sa_to_device(sa)
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for i in range(8):
+        with torch.cuda.stream(streams[i % 2]):
+            D = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+            g.fp8_gemm_nt(A, sAt, B, sBt, D)
+            outs.append(D)
+    torch.cuda.synchronize()
+    check_status()
+    for D in outs[1:]:
+        assert torch.equal(D, outs[0])

@@ -1,0 +1,125 @@
+"""GPU parity of the quantisation kernels against the oracle: bytes and scales bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_block_gb300 as g
+from moe_grouped_gemm_block_gb300.workloads import WORKLOADS, make_inputs
+from oracle import quantize_128x128, quantize_1x128
+from tests.gpu_util import check_status, need_gpu, sa_from_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    need_gpu()
+
+
+def _bf16(shape, seed, scale=1.0):
+    gen = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=gen) * scale).to(torch.bfloat16)
+
+
+def _np(x):
+    return x.float().numpy()
+
+
+def _check_1x128(x_cpu: torch.Tensor, rows=None):
+    q, sA = g.quantize_1x128(x_cpu.cuda())
+    torch.cuda.synchronize()
+    check_status()
+    M = x_cpu.shape[0]
+    rows = np.arange(M) if rows is None else rows
+    q_ref, s_ref = quantize_1x128(_np(x_cpu[rows]))
+    assert np.array_equal(q.cpu().numpy()[rows], q_ref)
+    s_gpu = sa_from_device(sA, M)[rows]
+    assert np.array_equal(s_gpu.view(np.uint32), s_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 384), (128, 512), (200, 1024), (64, 7168)])
+def test_1x128_small_shapes(M, K):
+    _check_1x128(_bf16((M, K), seed=M + K, scale=3.0))
+
+
+def test_1x128_edge_values():
+    x = torch.zeros((8, 256))
+    x[1, 0] = 448.0                    # s = 1: values map to themselves
+    # midpoints between neighbouring codes (ties to even), the subnormal step, signed zero
+    x[1, 1:8] = torch.tensor([1.0625, 1.1875, 0.0009765625, -0.0009765625, 2.0 ** -10, 432.0, -0.0])
+    x[1, 8] = -448.0
+    x[2, :128] = 1e-30                 # tiny block: s is subnormal in fp32
+    x[2, 5] = -3e-30
+    x[3, :] = -0.0                     # all (negative) zeros: s = 0, codes 0
+    x[4, :] = torch.linspace(-5, 5, 256)
+    x[5, 130] = 3.0e38                 # bf16-representable huge value
+    x[6, :128] = 2.0 ** -133           # smallest bf16 subnormal
+    x[7, ::7] = 1.0
+    x[7, 128] = 464.0                  # rounds past 448 before saturation when s = 1
+    _check_1x128(x.to(torch.bfloat16))
+
+
+def test_1x128_zero_rows_and_strided_layouts():
+    x = _bf16((40, 512), seed=7)
+    x[5] = 0
+    big = torch.zeros((40, 640), dtype=torch.bfloat16)
+    big[:, :512] = x
+    xs = big.cuda()[:, :512]  # ldx = 640
+    q = torch.full((40, 528), 0x55, dtype=torch.uint8, device="cuda")[:, :512]  # ldq = 528
+    sA = torch.full((4, 48), -1.0, device="cuda")  # ld_sa = 48 > M
+    g.fp8_quantize_1x128(xs, q, sA)
+    torch.cuda.synchronize()
+    check_status()
+    q_ref, s_ref = quantize_1x128(_np(x))
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sA[:, :40].cpu().numpy().T, s_ref)
+    assert torch.all(sA[:, 40:] == -1.0)  # entries past M untouched
+
+
+def test_1x128_m_zero_is_noop():
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((0, 256), dtype=torch.uint8, device="cuda")
+    sA = torch.empty((2, 4), device="cuda")
+    g.fp8_quantize_1x128(x, q, sA)
+    check_status()
+
+
+@pytest.mark.parametrize("name", ["decode", "large_4096", "moe_contiguous", "moe_masked"])
+def test_1x128_full_size_workloads(name):
+    w = WORKLOADS[name]
+    x = make_inputs(w, device="cuda")["A"]
+    x = x.reshape(-1, w.K)
+    q, sA = g.quantize_1x128(x)
+    torch.cuda.synchronize()
+    check_status()
+    M = x.shape[0]
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(M, min(M, 192), replace=False), [0, M - 1]]))
+    q_ref, s_ref = quantize_1x128(x[rows].float().cpu().numpy())
+    assert np.array_equal(q[rows].cpu().numpy(), q_ref)
+    assert np.array_equal(sa_from_device(sA, M)[rows], s_ref)
+
+
+@pytest.mark.parametrize("E,N,K", [(1, 128, 128), (2, 200, 384), (3, 16, 256), (1, 7168 // 8, 512)])
+def test_128x128_small_shapes(E, N, K):
+    w = _bf16((E, N, K), seed=E * N + K, scale=0.05)
+    q, sB = g.quantize_128x128(w.cuda())
+    torch.cuda.synchronize()
+    check_status()
+    for e in range(E):
+        q_ref, s_ref = quantize_128x128(_np(w[e]))
+        assert np.array_equal(q[e].cpu().numpy(), q_ref)
+        assert np.array_equal(sB[e].cpu().numpy(), s_ref)
+
+
+def test_128x128_full_size_masked_weights_sampled_experts():
+    w = WORKLOADS["moe_masked"]
+    B = make_inputs(w, device="cuda")["B"]
+    q, sB = g.quantize_128x128(B)
+    torch.cuda.synchronize()
+    check_status()
+    for e in (0, 17, w.E - 1):
+        q_ref, s_ref = quantize_128x128(B[e].float().cpu().numpy())
+        assert np.array_equal(q[e].cpu().numpy(), q_ref)
+        assert np.array_equal(sB[e].cpu().numpy(), s_ref)
