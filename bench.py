@@ -96,7 +96,7 @@ def barrier(dist):
 class ClockSampler:
     """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -104,6 +104,10 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.window = None  # (t0, t1) wall-clock seconds of the timed region
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -125,13 +129,22 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        import datetime
+
         rows = []
         try:
             with open(self.path) as f:
                 for line in f:
                     parts = [p.strip() for p in line.split(",")]
-                    if len(parts) >= 9:
-                        rows.append(parts)
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    if self.window and ts is not None and not (self.window[0] - 0.25 <= ts <= self.window[1] + 0.05):
+                        continue
+                    rows.append(parts[1:])
         except OSError:
             pass
         finally:
@@ -266,21 +279,22 @@ def run_ours(args, world, rank, local, dist):
             ev[2].record(stream)
             record.append((c.name, ev))
 
-    for _ in range(args.warmup):
-        one_step([])
-    torch.cuda.synchronize()
-
     launches_per_step = 2 * len(cases)
     records = []
-    barrier(dist)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk:  # started before the warm-up: nvidia-smi needs a moment
+        for _ in range(args.warmup):
+            one_step([])
+        torch.cuda.synchronize()
+        barrier(dist)
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
+        w0 = time.time()
         for _ in range(args.steps):
             one_step(records)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    barrier(dist)
+        clk.mark(w0, time.time())
+        barrier(dist)
     st = g.fp8g_get_status()
     if st != 0:
         raise RuntimeError(f"device status {g.STATUS.get(st, st)} after the timed region")
@@ -471,8 +485,8 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workloads", default=",".join(DEFAULT_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -72,7 +72,7 @@ typedef enum {
  *   q     e4m3 [M, K] (one byte each), row stride ldq bytes (ldq >= K, ldq % 16 == 0)
  *   sA    fp32 [K/128][ld_sa], K-block-major: sA[kb * ld_sa + m]
  *         (ld_sa >= M, ld_sa % 4 == 0; entries m >= M are not written)
- *   M >= 0 (M == 0: no-op), K > 0, K % 128 == 0.  Pointers 16-byte aligned.
+ *   M >= 0 (M == 0: no-op), K > 0, K % 128 == 0, M * (K/128) < 2^31.  Pointers 16-byte aligned.
  */
 int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
                        float* sA, int64_t ld_sa, void* stream);
@@ -125,7 +125,7 @@ int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa, cons
  *                 never reads it, so routing can stay on the GPU): non-decreasing,
  *                 each a multiple of 128, group_offsets[E] <= M_total.  Violations
  *                 make the kernel write nothing and set FP8G_ERR_DEVICE_ASSERT.
- *   1 <= E <= 4096, M_total >= 0 and M_total % 128 == 0, N % 16 == 0, K % 128 == 0.
+ *   1 <= E <= 2048, M_total >= 0 and M_total % 128 == 0, N % 16 == 0, K % 128 == 0.
  */
 int fp8_grouped_gemm_contiguous(const void* A, const float* sA, int64_t ld_sa, const void* B,
                                 const float* sB, void* D, const int32_t* group_offsets,
@@ -146,7 +146,7 @@ int fp8_grouped_gemm_contiguous(const void* A, const float* sA, int64_t ld_sa, c
  *   D         bf16 [E, cap, N], contiguous
  *   masked_m  int32 [E], DEVICE memory, 0 <= masked_m[e] <= cap; values outside are
  *             clamped into range and set FP8G_ERR_DEVICE_ASSERT.
- *   1 <= E <= 4096, cap >= 0 and cap % 16 == 0, N % 16 == 0, K % 128 == 0.
+ *   1 <= E <= 2048, cap >= 0 and cap % 16 == 0, N % 16 == 0, K % 128 == 0.
  */
 int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t ld_sa, const void* B,
                             const float* sB, void* D, const int32_t* masked_m, int32_t E,

@@ -45,8 +45,13 @@ constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a 
 template <int BN>
 struct Cfg {
   static constexpr int kEpiCols = BN >= 128 ? 128 : BN;  // columns per epilogue warp
-  static constexpr int kEpiGroups = BN / kEpiCols;       // warpgroups of epilogue warps
+  static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
+  // Narrow tiles (few, long K loops: small-M shapes) split the K blocks between two sets of
+  // promotion warps (even / odd K blocks), whose FP32 partial sums are added at the tile end.
+  static constexpr int kKSplit = BN == 64 ? 2 : 1;
+  static constexpr int kEpiGroups = kColGroups * kKSplit;  // warpgroups of epilogue warps
   static constexpr int kEpiWarps = 4 * kEpiGroups;
+  static constexpr int kStoreWarps = 4 * kColGroups;     // warps that write D
   // BN = 256: three full warpgroups (producer / MMA / 2 idle, then 2 epilogue warpgroups) so
   // that setmaxnreg can move registers to the epilogue: the launch gives 384 x 168 = 64512,
   // rebalanced to 128 x 40 + 256 x 232 = 64512.  Otherwise: 2 warps + 1 epilogue warpgroup.
@@ -54,19 +59,27 @@ struct Cfg {
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr bool kRebalance = BN == 256;
   static constexpr uint32_t kRegsLow = 40, kRegsHigh = 232;
-  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
+  // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
+  static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
+  static constexpr uint32_t kTmemCols = 512;
+  // Ring of A-row scales, separate from the operand stages: a stage is free once its MMAs
+  // are done, while a scale entry is held until the promotion warps have read it.
+  static constexpr int kSADepth = 2 * (kStages + kTmemBufs) > 16 ? 16 : 2 * (kStages + kTmemBufs);
   static constexpr uint32_t kABytes = BM * BK;
   static constexpr uint32_t kBBytes = BN * BK;
   static constexpr uint32_t kSABytes = BM * 4;
-  static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per warp
+  static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per store warp
+  static constexpr uint32_t kXBytes = kKSplit > 1 ? BM * BN * 4 : 0;  // K-split exchange
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
   static constexpr uint32_t kOffOut = kOffB + kStages * kBBytes;
-  static constexpr uint32_t kOffSA = kOffOut + kEpiWarps * kOutBytes;
-  static constexpr uint32_t kOffBar = kOffSA + kStages * kSABytes;
-  static constexpr uint32_t kNumBars = 2 * kStages + 4;
+  static constexpr uint32_t kOffX = kOffOut + kStoreWarps * kOutBytes;
+  static constexpr uint32_t kOffSA = kOffX + kXBytes;
+  static constexpr uint32_t kOffBar = kOffSA + kSADepth * kSABytes;
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kSADepth + 2 * kTmemBufs + 2;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
@@ -176,8 +189,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   const uint32_t bar0 = base + C::kOffBar;
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty = [&](uint32_t s) { return bar0 + 8u * (S + s); };
-  auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
-  auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 + b); };
+  constexpr uint32_t NB = C::kTmemBufs;
+  constexpr uint32_t SD = C::kSADepth;
+  auto safull = [&](uint32_t j) { return bar0 + 8u * (2 * S + j); };
+  auto saempty = [&](uint32_t j) { return bar0 + 8u * (2 * S + SD + j); };
+  auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 * SD + b); };
+  auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 * SD + NB + b); };
+  const uint32_t xfull = bar0 + 8u * (2 * S + 2 * SD + 2 * NB);  // K-split exchange written
+  const uint32_t xempty = xfull + 8u;                             // K-split exchange read
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);  // [0] tmem base, [1] abort
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   int32_t* table = reinterpret_cast<int32_t*>(smem + C::kOffTable);
@@ -185,12 +204,19 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1 + C::kEpiWarps);
+      mbar_init(empty(s), 1);
     }
-    for (uint32_t b = 0; b < 2; ++b) {
+    // each scale entry and TMEM buffer is consumed by the warps of one K part
+    for (uint32_t j = 0; j < SD; ++j) {
+      mbar_init(safull(j), 1);
+      mbar_init(saempty(j), C::kStoreWarps);
+    }
+    for (uint32_t b = 0; b < NB; ++b) {
       mbar_init(tfull(b), 1);
-      mbar_init(tempty(b), C::kEpiWarps);
+      mbar_init(tempty(b), C::kStoreWarps);
     }
+    mbar_init(xfull, C::kStoreWarps);
+    mbar_init(xempty, C::kStoreWarps);
     misc[1] = 0;
     misc[2] = 0;  // set when the group table is out of contract
     fence_mbar_init();
@@ -261,18 +287,23 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
         for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
+          const uint32_t j = it % SD, jph = (it / SD) & 1u;
           if (!wait_bounded(empty(s), ph ^ 1u, a, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes + C::kSABytes);
+          if (!wait_bounded(saempty(j), jph ^ 1u, a, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes);
           tma_load_2d(base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
           tma_load_3d(base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
-          tma_load_2d(base + C::kOffSA + s * C::kSABytes, &tmSA, full(s), ti.a_row, kb);
+          mbar_arrive_expect_tx(safull(j), C::kSABytes);
+          tma_load_2d(base + C::kOffSA + j * C::kSABytes, &tmSA, safull(j), ti.a_row, kb);
         }
       }
       if (!ok) {  // let the loads already issued land before the CTA exits
         const uint32_t n = it < S ? it : S;
         for (uint32_t i = it - n; i < it; ++i) {
           const long long t0 = clock64();
-          while (!mbar_try_wait(full(i % S), (i / S) & 1u) && clock64() - t0 < a.budget) {
+          while ((!mbar_try_wait(full(i % S), (i / S) & 1u) ||
+                  !mbar_try_wait(safull(i % SD), (i / SD) & 1u)) &&
+                 clock64() - t0 < a.budget) {
           }
         }
       }
@@ -288,7 +319,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
         for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          const uint32_t b = it & 1u, tph = (it >> 1) & 1u;
+          const uint32_t b = it % NB, tph = (it / NB) & 1u;
           if (!wait_bounded(tempty(b), tph ^ 1u, a, abort_flag)) { ok = false; break; }
           if (!wait_bounded(full(s), ph, a, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -307,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       if (!ok && it > 0) {  // wait for the MMAs already issued before TMEM is released
         const uint32_t last = it - 1;
         const long long t0 = clock64();
-        while (!mbar_try_wait(tfull(last & 1u), (last >> 1) & 1u) && clock64() - t0 < a.budget) {
+        while (!mbar_try_wait(tfull(last % NB), (last / NB) & 1u) && clock64() - t0 < a.budget) {
         }
       }
     }
@@ -317,10 +348,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     // ------------------------------------------------------------ promotion + epilogue
     const int ew = warp - C::kEpiWarp0;  // epilogue warp index
     const int q = warp & 3;              // TMEM lane quarter this warp may access
-    const int col0 = (ew >> 2) * C::kEpiCols;  // column offset of this warp inside the tile
+    const int grp = ew >> 2;             // epilogue warpgroup
+    const int kpart = grp / C::kColGroups;                 // promotes K blocks kb % kKSplit == kpart
+    const int col0 = (grp % C::kColGroups) * C::kEpiCols;  // column offset inside the tile
     const int row = q * 32 + lane;       // tile row owned by this thread
-    const uint32_t out_addr = base + C::kOffOut + ew * C::kOutBytes;
-    uint32_t it = 0;
+    const uint32_t out_addr = base + C::kOffOut + (ew % C::kStoreWarps) * C::kOutBytes;
+    float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
+    uint32_t it_base = 0, tiles_done = 0;
     bool ok = true;
     for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       Tile ti;
@@ -328,34 +362,68 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int32_t ncol0 = ti.n0 + col0;
       const bool has_cols = ncol0 < a.N;
       const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
-      float acc[C::kEpiCols];
+      // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
+      // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
+      int32_t sb_base = 0;
+      float sb_cur = (has_cols && lane < a.KB) ? ld_nc_f32(sbp + lane) : 0.0f;
+      float sb_nxt = (has_cols && lane + 32 < a.KB) ? ld_nc_f32(sbp + 32 + lane) : 0.0f;
+      float2 acc[C::kEpiCols / 2];
 #pragma unroll
-      for (int j = 0; j < C::kEpiCols; ++j) acc[j] = 0.0f;
-      float sb_next = has_cols ? ld_nc_f32(sbp) : 0.0f;
-      for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
-        const uint32_t s = it % S, ph = (it / S) & 1u;
-        const uint32_t b = it & 1u, tph = (it >> 1) & 1u;
-        const float sb_cur = sb_next;
-        if (has_cols && kb + 1 < a.KB) sb_next = ld_nc_f32(sbp + kb + 1);
-        if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
-        const float scale = sSA[s * BM + row] * sb_cur;
+      for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      for (int32_t kb = kpart; kb < a.KB; kb += C::kKSplit) {
+        const uint32_t it = it_base + kb;
+        const uint32_t j = it % SD, jph = (it / SD) & 1u;
+        const uint32_t b = it % NB, tph = (it / NB) & 1u;
+        if (kb >= sb_base + 32) {
+          sb_base += 32;
+          sb_cur = sb_nxt;
+          sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
+        }
+        const float sb_kb = __shfl_sync(0xffffffffu, sb_cur, kb - sb_base);
+        if (!__all_sync(0xffffffffu, wait_bounded(safull(j), jph, a, abort_flag))) { ok = false; break; }
+        const float scale = sSA[j * BM + row] * sb_kb;
+        const float2 scale2 = make_float2(scale, scale);
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty(s));
+        if (lane == 0) mbar_arrive(saempty(j));
         if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
 #pragma unroll
-        for (int c = 0; c < C::kEpiCols / 32; ++c) {
-          float v[32];
-          tmem_ld32_sync(taddr + c * 32, v);
+        for (int c = 0; c < C::kEpiCols / 64; ++c) {
+          float v[64];
+          tmem_ld64_sync(taddr + c * 64, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(v[j], scale, acc[c * 32 + j]);
+          for (int i = 0; i < 32; ++i)
+            acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty(b));
       }
+      it_base += a.KB;
       if (!ok) break;
+      if constexpr (C::kKSplit > 1) {
+        // add the odd-K-block partial sums (second warpgroup) into the first warpgroup's
+        const uint32_t xph = tiles_done & 1u;
+        ++tiles_done;
+        if (kpart == 1) {
+          if (!__all_sync(0xffffffffu, wait_bounded(xempty, xph ^ 1u, a, abort_flag))) { ok = false; break; }
+#pragma unroll
+          for (int i = 0; i < C::kEpiCols / 2; ++i) xbuf[i * BM + row] = acc[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xfull);
+          continue;
+        }
+        if (!__all_sync(0xffffffffu, wait_bounded(xfull, xph, a, abort_flag))) { ok = false; break; }
+#pragma unroll
+        for (int i = 0; i < C::kEpiCols / 2; ++i) {
+          const float2 o = xbuf[i * BM + row];
+          acc[i].x += o.x;
+          acc[i].y += o.y;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xempty);
+      }
       // ---- epilogue: this warp holds rows q*32 .. q*32+31, columns ncol0 .. ncol0+kEpiCols-1
       const int nvalid = min(32, ti.rows - q * 32);
       if (nvalid <= 0 || !has_cols) continue;
@@ -367,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           __syncwarp();
           uint32_t p[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(acc[32 * j + 2 * i], acc[32 * j + 2 * i + 1]);
+          for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(acc[16 * j + i].x, acc[16 * j + i].y);
           const uint32_t rowaddr = out_addr + lane * 64;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -389,10 +457,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         for (int j = 0; j < C::kEpiCols / 8; ++j) {
           if (ncol0 + 8 * j < a.N) {
             uint4 v;
-            v.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
-            v.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
-            v.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
-            v.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+            v.x = pack_bf16x2(acc[4 * j + 0].x, acc[4 * j + 0].y);
+            v.y = pack_bf16x2(acc[4 * j + 1].x, acc[4 * j + 1].y);
+            v.z = pack_bf16x2(acc[4 * j + 2].x, acc[4 * j + 2].y);
+            v.w = pack_bf16x2(acc[4 * j + 3].x, acc[4 * j + 3].y);
             *reinterpret_cast<uint4*>(drow + 8 * j) = v;
           }
         }
@@ -414,7 +482,11 @@ constexpr uint32_t smem_bytes(int table_entries) {
   return Cfg<BN>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
 }
 
-constexpr int kMaxExperts = 4096;
+constexpr int kMaxExperts = 2048;
+constexpr uint32_t kSmemLimit = 232448;  // 227 KB: the per-block dynamic shared memory limit
+static_assert(Cfg<256>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 
 template <int BN, int MODE>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
@@ -581,11 +653,12 @@ using namespace fp8g;
 extern "C" int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa,
                            const void* B, int64_t ldb, const float* sB, void* D, int64_t ldd,
                            int64_t M, int64_t N, int64_t K, void* stream) {
-  if (!A || !sA || !B || !sB || !D) return FP8G_ERR_INVALID_ARG;
   if (M < 0 || M > kMaxI32 || N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 ||
       K > kMaxI32)
     return FP8G_ERR_INVALID_ARG;
   if (lda < K || ldb < K || ldd < N || ld_sa < M) return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;  // nothing to do; the pointers of empty tensors may be null
+  if (!A || !sA || !B || !sB || !D) return FP8G_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
       lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0 || ld_sa % 4 != 0)
     return FP8G_ERR_ALIGNMENT;
@@ -597,11 +670,12 @@ extern "C" int fp8_grouped_gemm_contiguous(const void* A, const float* sA, int64
                                            const void* B, const float* sB, void* D,
                                            const int32_t* group_offsets, int32_t E,
                                            int64_t M_total, int64_t N, int64_t K, void* stream) {
-  if (!A || !sA || !B || !sB || !D || !group_offsets) return FP8G_ERR_INVALID_ARG;
   if (E < 1 || E > kMaxExperts || M_total < 0 || M_total > kMaxI32 || M_total % 128 != 0 ||
       N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32 ||
-      ld_sa < M_total || N * E > kMaxI32 * 64)
+      ld_sa < M_total)
     return FP8G_ERR_INVALID_ARG;
+  if (M_total == 0) return FP8G_OK;
+  if (!A || !sA || !B || !sB || !D || !group_offsets) return FP8G_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
       (reinterpret_cast<uintptr_t>(group_offsets) & 3u) || ld_sa % 4 != 0)
     return FP8G_ERR_ALIGNMENT;
@@ -613,11 +687,12 @@ extern "C" int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t l
                                        const void* B, const float* sB, void* D,
                                        const int32_t* masked_m, int32_t E, int64_t cap, int64_t N,
                                        int64_t K, void* stream) {
-  if (!A || !sA || !B || !sB || !D || !masked_m) return FP8G_ERR_INVALID_ARG;
   if (E < 1 || E > kMaxExperts || cap < 0 || cap % 16 != 0 || static_cast<int64_t>(E) * cap > kMaxI32 ||
       N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32 ||
       ld_sa < static_cast<int64_t>(E) * cap)
     return FP8G_ERR_INVALID_ARG;
+  if (cap == 0) return FP8G_OK;
+  if (!A || !sA || !B || !sB || !D || !masked_m) return FP8G_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
       (reinterpret_cast<uintptr_t>(masked_m) & 3u) || ld_sa % 4 != 0)
     return FP8G_ERR_ALIGNMENT;

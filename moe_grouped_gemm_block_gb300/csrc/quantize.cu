@@ -6,8 +6,9 @@
 // weights one per 128x128 block (explainer sec. 5.1).
 //
 // Both kernels are HBM-bound (2 bytes read + 1 byte written per element): 16-byte
-// coalesced loads, 8-byte coalesced stores, IEEE division (__fdiv_rn) and the
-// round-to-nearest-even saturating e4m3 conversion.
+// coalesced loads, 8-byte coalesced stores, the e4m3 code of the IEEE fp32 quotient x / s
+// (a multiplication by 1/s, with the division kept for the rare elements where the two
+// could round differently) and the round-to-nearest-even saturating e4m3 conversion.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,57 +37,107 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
   return m;
 }
 
-// 8 values / s -> 8 e4m3 bytes (little-endian: value 0 in the lowest byte).
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
-  if (s == 0.0f) return make_uint2(0u, 0u);
-  uint32_t w[2];
+// The e4m3 codes of the IEEE quotients x / s, without a division for almost every element.
+//
+// y = RN(x * r) with r = RN(1/s) differs from the exact quotient q by less than 2^-23 |q|,
+// so y and RN(q) are less than 3 ulps apart.  In e4m3's normal range (|y| >= 2^-6) the
+// rounding keeps 3 mantissa bits, and its decision points (the midpoints between
+// neighbouring codes) are the fp32 values whose low 20 mantissa bits are 0x80000.  When y
+// is more than 8 ulps from such a point, y and RN(q) round to the same code.  Elements
+// closer than that, and those below 2^-6 (where the code spacing is a fixed 2^-9), take
+// the IEEE division; so does everything when s is not a normal number (r inexact).
+__device__ __forceinline__ bool near_boundary(float y) {
+  const uint32_t u = __float_as_uint(y) & 0x7FFFFFFFu;
+  const bool small = (u - 1u) < 0x3C7FFFFFu;          // 0 < |y| < 2^-6
+  const bool mid = ((u & 0xFFFFFu) - 0x7FFF8u) < 17u;  // low 20 bits within 8 of 0x80000
+  return small || mid;
+}
+
+// N values / s -> N e4m3 codes, little-endian (value 0 in the lowest byte of w[0]).
+template <int N>
+__device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (&w)[N / 4]) {
+  if (s == 0.0f) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint16_t lo = cvt_e4m3x2(__fdiv_rn(f[4 * i + 1], s), __fdiv_rn(f[4 * i + 0], s));
-    const uint16_t hi = cvt_e4m3x2(__fdiv_rn(f[4 * i + 3], s), __fdiv_rn(f[4 * i + 2], s));
+    for (int i = 0; i < N / 4; ++i) w[i] = 0u;
+    return;
+  }
+  const float r = __frcp_rn(s);
+  const bool exact_all = !(s >= 1.17549435e-38f);  // subnormal s: divide every element
+  float y[N];
+  uint32_t redo = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    y[i] = __fmul_rn(f[i], r);
+    redo |= (exact_all || near_boundary(y[i])) ? (1u << i) : 0u;
+  }
+  if (redo != 0u) {  // rare: the IEEE division decides these elements
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (redo & (1u << i)) y[i] = __fdiv_rn(f[i], s);
+  }
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i) {
+    const uint16_t lo = cvt_e4m3x2(y[4 * i + 1], y[4 * i]), hi = cvt_e4m3x2(y[4 * i + 3], y[4 * i + 2]);
     w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
+}
+
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  uint32_t w[2];
+  quant_n<8>(f, s, w);
   return make_uint2(w[0], w[1]);
 }
 
-// One half-warp (16 lanes x 8 values) per (row, 128-wide K block).  Each thread keeps
-// UNROLL items in flight to cover HBM latency.
+// Eight lanes per (row, 128-wide K block); lane i of the group holds values 8i..8i+7 and
+// 64+8i..64+8i+7, so each 16-byte load instruction of a warp reads four whole 128-byte
+// lines.  Each group keeps kQUnroll blocks in flight to cover HBM latency.
 constexpr int kQThreads = 256;
 constexpr int kQUnroll = 2;
 
 __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
-    const __nv_bfloat16* __restrict__ x, int64_t M, int64_t KB, int64_t ldx,
+    const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa) {
-  const int lane = threadIdx.x & 31;
-  const int sub = lane & 15;
-  const int64_t half_id = (static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x) >> 4;
-  const int64_t n_halves = static_cast<int64_t>(gridDim.x) * (kQThreads >> 4);
-  const int64_t total = M * KB;
-  for (int64_t base = half_id; base - half_id < total; base += n_halves * kQUnroll) {
-    uint4 raw[kQUnroll];
-    int64_t item[kQUnroll];
+  const int sub = threadIdx.x & 7;
+  const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) >> 3;
+  const uint32_t n_groups = gridDim.x * (kQThreads >> 3);
+  const uint32_t total = M * KB;  // the host guarantees M * KB < 2^31
+  for (uint32_t base = group; base - group < total; base += n_groups * kQUnroll) {
+    uint4 raw[kQUnroll][2];
+    uint32_t m[kQUnroll], kb[kQUnroll];
 #pragma unroll
     for (int u = 0; u < kQUnroll; ++u) {
-      item[u] = base + static_cast<int64_t>(u) * n_halves;
-      raw[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (item[u] < total) {
-        const int64_t m = item[u] / KB, kb = item[u] - m * KB;
-        raw[u] = __ldg(reinterpret_cast<const uint4*>(x + m * ldx + kb * 128 + sub * 8));
+      const uint32_t item = base + u * n_groups;
+      m[u] = item / KB;
+      kb[u] = item - m[u] * KB;
+      raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (item < total) {
+        const __nv_bfloat16* src = x + m[u] * ldx + kb[u] * 128 + sub * 8;
+        raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
+        raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 64));
       }
     }
 #pragma unroll
     for (int u = 0; u < kQUnroll; ++u) {
-      float f[8];
-      unpack8(raw[u], f);
-      float a = amax8(f);
-      // reduce over the 16 lanes of this half-warp (xor offsets < 16 stay inside it)
+      float f[16], lo[8], hi[8];
+      unpack8(raw[u][0], lo);
+      unpack8(raw[u][1], hi);
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+      for (int i = 0; i < 8; ++i) {
+        f[i] = lo[i];
+        f[8 + i] = hi[i];
+      }
+      float a = fmaxf(amax8(lo), amax8(hi));
+      // reduce over the 8 lanes of this group (xor offsets < 8 stay inside it)
+#pragma unroll
+      for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
       const float s = __fdiv_rn(a, kE4M3Max);
-      if (item[u] < total) {
-        const int64_t m = item[u] / KB, kb = item[u] - m * KB;
-        *reinterpret_cast<uint2*>(q + m * ldq + kb * 128 + sub * 8) = quant8(f, s);
-        if (sub == 0) sA[kb * ld_sa + m] = s;
+      if (base + u * n_groups < total) {
+        uint32_t c[4];
+        quant_n<16>(f, s, c);
+        uint8_t* dst = q + m[u] * ldq + kb[u] * 128 + sub * 8;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+        *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
+        if (sub == 0) sA[kb[u] * ld_sa + m[u]] = s;
       }
     }
   }
@@ -145,6 +196,7 @@ extern "C" int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t l
                                   int64_t ldq, float* sA, int64_t ld_sa, void* stream) {
   if (M < 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq < K || ld_sa < M)
     return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;  // nothing to do; the pointers of empty tensors may be null
   if (!x || !q || !sA) return FP8G_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sA) || ldx % 8 != 0 || ldq % 16 != 0 ||
       ld_sa % 4 != 0)
@@ -152,16 +204,16 @@ extern "C" int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t l
   DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
   if (st != FP8G_OK) return st;
-  if (M == 0) return FP8G_OK;
   const int64_t items = M * (K / 128);
-  const int64_t per_block = (kQThreads / 16) * kQUnroll;
+  if (items >= (int64_t{1} << 31) || M > 0x7FFFFFFF) return FP8G_ERR_INVALID_ARG;
+  const int64_t per_block = (kQThreads / 8) * kQUnroll;
   int64_t blocks = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
   if (blocks > cap) blocks = cap;
   quantize_1x128_kernel<<<static_cast<unsigned>(blocks), kQThreads, 0,
                           static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(x), M, K / 128, ldx, static_cast<uint8_t*>(q), ldq, sA,
-      ld_sa);
+      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx,
+      static_cast<uint8_t*>(q), ldq, sA, ld_sa);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

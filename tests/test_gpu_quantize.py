@@ -123,3 +123,26 @@ def test_128x128_full_size_masked_weights_sampled_experts():
         q_ref, s_ref = quantize_128x128(B[e].float().cpu().numpy())
         assert np.array_equal(q[e].cpu().numpy(), q_ref)
         assert np.array_equal(sB[e].cpu().numpy(), s_ref)
+
+
+def test_1x128_quotients_on_every_rounding_midpoint():
+    # amax = 448 * 2^k makes s = 2^k, so x / s is exact: blocks full of e4m3 midpoints (ties to
+    # even) and of their bf16 neighbours exercise both the multiply path and the division path.
+    tab = [(1 + m / 8) * 2.0 ** (e - 7) for e in range(1, 16) for m in range(8)]
+    tab = [v for v in tab if v <= 448]
+    mids = [(a + b) / 2 for a, b in zip(tab[:-1], tab[1:])]
+    vals = torch.tensor(mids + [2.0 ** -10, 3 * 2.0 ** -11, 2.0 ** -7 + 2.0 ** -10])
+    rows = []
+    for k in (-20, -3, 0, 5, 30):
+        for nudge in (0, 1, -1):  # the midpoint and its bf16 neighbours
+            blk = torch.zeros(128)
+            v = vals.to(torch.bfloat16)
+            if nudge:
+                v = (v.view(torch.int16) + nudge).view(torch.bfloat16)
+            v = v.float()
+            blk[:v.numel()] = v
+            blk[127] = 448.0
+            sign = torch.where(torch.arange(128) % 2 == 0, 1.0, -1.0)
+            rows.append(blk * sign * 2.0 ** k)
+    x = torch.stack(rows).to(torch.bfloat16)
+    _check_1x128(x)
