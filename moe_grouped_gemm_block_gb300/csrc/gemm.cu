@@ -7,18 +7,21 @@
 // GEMM pipeline, not by a separate dequantisation pass.
 //
 // GB300 design (one CTA per SM, persistent over output tiles of 128 x BN):
-//   warp 0        TMA producer: A tile (128 x 128 B), B tile (BN x 128 B), the 128 A-row
-//                 scales of the K block -> one stage of a STAGES-deep shared-memory ring,
-//                 signalled through a full/empty mbarrier pair per stage.
+//   warp 0        TMA producer: A tile (128 x 128 B) and B tile (BN x 128 B) of each K block
+//                 into one stage of a STAGES-deep shared-memory ring, signalled through a
+//                 full/empty mbarrier pair per stage (two TMA instructions per K block).
 //   warp 1        allocates TMEM; one lane issues 4 tcgen05.mma kind::f8f6f4 (K = 32 each)
 //                 per K block into a FRESH TMEM partial (the first MMA does not accumulate),
-//                 double-buffered (2 x BN columns) so the MMA of block kb+1 overlaps the
-//                 promotion of block kb.
-//   warps 2..     promotion + epilogue: tcgen05.ld the partial, acc = fma(P, sa*sb, acc) in
-//                 FP32 registers (one TMEM lane = one output row per thread), then after the
-//                 last K block convert to BF16 and store through shared memory with TMA
-//                 (64-byte-swizzled 32 x 32 boxes).  Rows past a masked expert's count are
-//                 never written.
+//                 in a ring of TMEM buffers (2 at BN = 256, up to 8 for narrow tiles) so the
+//                 MMA of later K blocks overlaps the promotion of earlier ones.
+//   warps 2.. /4..  promotion + epilogue: tcgen05.ld the partial (64 columns per load), then
+//                 acc = fma(P, sa*sb, acc) in FP32 registers with packed FP32 FMAs (one TMEM
+//                 lane = one output row per thread).  sa (one per row and K block) is read
+//                 from global memory a few K blocks ahead; sb (one per 128 columns and K
+//                 block) is held in a register per lane and broadcast by shuffle.  After the
+//                 last K block: BF16, staged in shared memory, stored with TMA (64-byte
+//                 swizzled 32 x 32 boxes).  Rows past a masked expert's count are never
+//                 written.  Narrow tiles (BN = 64) split the K blocks between two warpgroups.
 // Every wait is bounded: a wait that runs past its cycle budget records FP8G_ERR_TIMEOUT in
 // the status word, raises a shared abort flag, and every role returns.
 
@@ -36,13 +39,15 @@
 namespace fp8g {
 namespace {
 
-enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+// kDenseSmallM: dense with M <= 64 (decode shapes), BN = 64 only: loads 64 A rows per stage.
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3 };
 
 constexpr int BM = 128;  // rows per tile = TMEM lanes
 constexpr int BK = 128;  // K per stage = the scaling block
 constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a band)
+constexpr int kSAAhead = 4;  // K-block steps by which the A-row scales are loaded ahead
 
-template <int BN>
+template <int BN, bool SMALL = false>
 struct Cfg {
   static constexpr int kEpiCols = BN >= 128 ? 128 : BN;  // columns per epilogue warp
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
@@ -59,31 +64,31 @@ struct Cfg {
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr bool kRebalance = BN == 256;
   static constexpr uint32_t kRegsLow = 40, kRegsHigh = 232;
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  // A rows loaded per stage: the MMA always reads 128 rows, and with SMALL the upper 64 are
+  // whatever follows in shared memory (those rows of D are computed but never stored).
+  static constexpr int kARows = SMALL ? 64 : BM;
+  static constexpr int kStages = SMALL ? 12 : (BN == 256 ? 4 : 6);
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
   static constexpr uint32_t kTmemCols = 512;
-  // Ring of A-row scales, separate from the operand stages: a stage is free once its MMAs
-  // are done, while a scale entry is held until the promotion warps have read it.
-  static constexpr int kSADepth = 2 * (kStages + kTmemBufs) > 16 ? 16 : 2 * (kStages + kTmemBufs);
-  static constexpr uint32_t kABytes = BM * BK;
+  static constexpr uint32_t kABytes = kARows * BK;
   static constexpr uint32_t kBBytes = BN * BK;
-  static constexpr uint32_t kSABytes = BM * 4;
   static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per store warp
-  static constexpr uint32_t kXBytes = kKSplit > 1 ? BM * BN * 4 : 0;  // K-split exchange
+  static constexpr int kXRows = SMALL ? 64 : BM;
+  static constexpr uint32_t kXBytes = kKSplit > 1 ? kXRows * BN * 4 : 0;  // K-split exchange
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
   static constexpr uint32_t kOffOut = kOffB + kStages * kBBytes;
   static constexpr uint32_t kOffX = kOffOut + kStoreWarps * kOutBytes;
-  static constexpr uint32_t kOffSA = kOffX + kXBytes;
-  static constexpr uint32_t kOffBar = kOffSA + kSADepth * kSABytes;
-  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kSADepth + 2 * kTmemBufs + 2;
+  static constexpr uint32_t kOffBar = kOffX + kXBytes;
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kTmemBufs + 2;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+  static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
 };
 
 struct GemmArgs {
@@ -92,6 +97,8 @@ struct GemmArgs {
   int32_t num_m;     // m-blocks (dense / contiguous)
   int32_t num_n;     // n-blocks of BN
   int32_t num_tiles; // dense / contiguous tile count
+  const float* sA;   // A-row scales [KB][ld_sa]
+  int64_t ld_sa;
   const float* sB;
   __nv_bfloat16* D;
   int64_t ldd;
@@ -172,11 +179,11 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 }
 
 template <int BN, int MODE>
-__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
+                    const __grid_constant__ CUtensorMap tmD,
                     const GemmArgs a) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MODE == kDenseSmallM>;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_u32(smem);
@@ -185,17 +192,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sSA = reinterpret_cast<float*>(smem + C::kOffSA);
   const uint32_t bar0 = base + C::kOffBar;
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty = [&](uint32_t s) { return bar0 + 8u * (S + s); };
   constexpr uint32_t NB = C::kTmemBufs;
-  constexpr uint32_t SD = C::kSADepth;
-  auto safull = [&](uint32_t j) { return bar0 + 8u * (2 * S + j); };
-  auto saempty = [&](uint32_t j) { return bar0 + 8u * (2 * S + SD + j); };
-  auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 * SD + b); };
-  auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 * SD + NB + b); };
-  const uint32_t xfull = bar0 + 8u * (2 * S + 2 * SD + 2 * NB);  // K-split exchange written
+  auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + NB + b); };
+  const uint32_t xfull = bar0 + 8u * (2 * S + 2 * NB);  // K-split exchange written
   const uint32_t xempty = xfull + 8u;                             // K-split exchange read
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);  // [0] tmem base, [1] abort
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -206,11 +209,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    // each scale entry and TMEM buffer is consumed by the warps of one K part
-    for (uint32_t j = 0; j < SD; ++j) {
-      mbar_init(safull(j), 1);
-      mbar_init(saempty(j), C::kStoreWarps);
-    }
+    // each TMEM buffer is consumed by the warps of one K part
     for (uint32_t b = 0; b < NB; ++b) {
       mbar_init(tfull(b), 1);
       mbar_init(tempty(b), C::kStoreWarps);
@@ -222,7 +221,6 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    prefetch_tmap(&tmSA);
     prefetch_tmap(&tmD);
   }
   if (warp == 1) {
@@ -277,9 +275,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   if (MODE == kContiguous && misc[2]) num_tiles = 0;
   if (warp < C::kEpiWarp0) {
     if constexpr (C::kRebalance) regs_release<C::kRegsLow>();
+    // Producer and MMA warps: all 32 lanes run the loop (warp-uniform control flow and
+    // operands); lane 0 alone issues the TMA copies, the MMAs and the commits.
+    const bool leader = lane == 0;
     if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       uint32_t it = 0;
       bool ok = true;
       for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -287,31 +287,27 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
         for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          const uint32_t j = it % SD, jph = (it / SD) & 1u;
-          if (!wait_bounded(empty(s), ph ^ 1u, a, abort_flag)) { ok = false; break; }
-          if (!wait_bounded(saempty(j), jph ^ 1u, a, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes);
-          tma_load_2d(base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
-          tma_load_3d(base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
-          mbar_arrive_expect_tx(safull(j), C::kSABytes);
-          tma_load_2d(base + C::kOffSA + j * C::kSABytes, &tmSA, safull(j), ti.a_row, kb);
+          if (!__all_sync(0xffffffffu, wait_bounded(empty(s), ph ^ 1u, a, abort_flag))) { ok = false; break; }
+          mbar_arrive_expect_tx_if(leader, full(s), C::kABytes + C::kBBytes);
+          tma_load_2d_if(leader, base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
+          tma_load_3d_if(leader, base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
         }
       }
-      if (!ok) {  // let the loads already issued land before the CTA exits
+      if (!ok && leader) {  // let the loads already issued land before the CTA exits
         const uint32_t n = it < S ? it : S;
         for (uint32_t i = it - n; i < it; ++i) {
           const long long t0 = clock64();
-          while ((!mbar_try_wait(full(i % S), (i / S) & 1u) ||
-                  !mbar_try_wait(safull(i % SD), (i / SD) & 1u)) &&
-                 clock64() - t0 < a.budget) {
+          while (!mbar_try_wait(full(i % S), (i / S) & 1u) && clock64() - t0 < a.budget) {
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      // descriptors of stage 0; stage s and K step k add (offset in bytes) / 16 to the
+      // 14-bit start-address field (shared addresses stay below 2^18, so it cannot carry)
+      const uint64_t adesc0 = smem_desc_k_sw128(base + C::kOffA);
+      const uint64_t bdesc0 = smem_desc_k_sw128(base + C::kOffB);
       uint32_t it = 0;
       bool ok = true;
       for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -320,29 +316,26 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           const uint32_t b = it % NB, tph = (it / NB) & 1u;
-          if (!wait_bounded(tempty(b), tph ^ 1u, a, abort_flag)) { ok = false; break; }
-          if (!wait_bounded(full(s), ph, a, abort_flag)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = base + C::kOffA + s * C::kABytes;
-          const uint32_t b_addr = base + C::kOffB + s * C::kBBytes;
+          const uint64_t ad = adesc0 + ((s * C::kABytes) >> 4);
+          const uint64_t bd = bdesc0 + ((s * C::kBBytes) >> 4);
           const uint32_t d_tmem = tmem_base + b * BN;
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k) {
-            mma_f8f6f4(d_tmem, smem_desc_k_sw128(a_addr + 32 * k), smem_desc_k_sw128(b_addr + 32 * k),
-                       idesc, k > 0 ? 1u : 0u);
-          }
-          mma_commit(empty(s));
-          mma_commit(tfull(b));
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8f6f4_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+          mma_commit_if(leader, empty(s));
+          mma_commit_if(leader, tfull(b));
         }
       }
-      if (!ok && it > 0) {  // wait for the MMAs already issued before TMEM is released
+      if (!ok && it > 0 && leader) {  // wait for the MMAs already issued before TMEM is released
         const uint32_t last = it - 1;
         const long long t0 = clock64();
         while (!mbar_try_wait(tfull(last % NB), (last / NB) & 1u) && clock64() - t0 < a.budget) {
         }
       }
     }
-  }
   } else {
     if constexpr (C::kRebalance) regs_acquire<C::kRegsHigh>();
     // ------------------------------------------------------------ promotion + epilogue
@@ -361,40 +354,59 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
       const int32_t ncol0 = ti.n0 + col0;
       const bool has_cols = ncol0 < a.N;
+      // small-M tiles: warps whose rows are all past M skip the promotion (nothing to store)
+      const bool live = MODE != kDenseSmallM || q * 32 < ti.rows;
       const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
       // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
       // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
       int32_t sb_base = 0;
       float sb_cur = (has_cols && lane < a.KB) ? ld_nc_f32(sbp + lane) : 0.0f;
       float sb_nxt = (has_cols && lane + 32 < a.KB) ? ld_nc_f32(sbp + 32 + lane) : 0.0f;
+      // A-row scale of this thread's row, read from global memory kSAAhead K-block steps
+      // before use (coalesced: a warp reads 32 consecutive rows of one K block)
+      const int32_t grow = ti.a_row + row;
+      const bool row_ok = grow < a.rows;
+      const float* sap = a.sA + grow;
+      float sa_q[kSAAhead];
+#pragma unroll
+      for (int i = 0; i < kSAAhead; ++i) {
+        const int32_t kbi = kpart + i * C::kKSplit;
+        sa_q[i] = (row_ok && kbi < a.KB) ? ld_nc_f32(sap + static_cast<int64_t>(kbi) * a.ld_sa) : 0.0f;
+      }
       float2 acc[C::kEpiCols / 2];
 #pragma unroll
       for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       for (int32_t kb = kpart; kb < a.KB; kb += C::kKSplit) {
         const uint32_t it = it_base + kb;
-        const uint32_t j = it % SD, jph = (it / SD) & 1u;
         const uint32_t b = it % NB, tph = (it / NB) & 1u;
+        const float sa_kb = sa_q[0];
+#pragma unroll
+        for (int i = 0; i + 1 < kSAAhead; ++i) sa_q[i] = sa_q[i + 1];
+        {
+          const int32_t kbn = kb + kSAAhead * C::kKSplit;
+          sa_q[kSAAhead - 1] =
+              (row_ok && kbn < a.KB) ? ld_nc_f32(sap + static_cast<int64_t>(kbn) * a.ld_sa) : 0.0f;
+        }
         if (kb >= sb_base + 32) {
           sb_base += 32;
           sb_cur = sb_nxt;
           sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
         }
         const float sb_kb = __shfl_sync(0xffffffffu, sb_cur, kb - sb_base);
-        if (!__all_sync(0xffffffffu, wait_bounded(safull(j), jph, a, abort_flag))) { ok = false; break; }
-        const float scale = sSA[j * BM + row] * sb_kb;
+        const float scale = sa_kb * sb_kb;
         const float2 scale2 = make_float2(scale, scale);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(saempty(j));
         if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
+        if (live) {
 #pragma unroll
-        for (int c = 0; c < C::kEpiCols / 64; ++c) {
-          float v[64];
-          tmem_ld64_sync(taddr + c * 64, v);
+          for (int c = 0; c < C::kEpiCols / 64; ++c) {
+            float v[64];
+            tmem_ld64_sync(taddr + c * 64, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+            for (int i = 0; i < 32; ++i)
+              acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -408,18 +420,22 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         ++tiles_done;
         if (kpart == 1) {
           if (!__all_sync(0xffffffffu, wait_bounded(xempty, xph ^ 1u, a, abort_flag))) { ok = false; break; }
+          if (live) {
 #pragma unroll
-          for (int i = 0; i < C::kEpiCols / 2; ++i) xbuf[i * BM + row] = acc[i];
+            for (int i = 0; i < C::kEpiCols / 2; ++i) xbuf[i * C::kXRows + row] = acc[i];
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(xfull);
           continue;
         }
         if (!__all_sync(0xffffffffu, wait_bounded(xfull, xph, a, abort_flag))) { ok = false; break; }
+        if (live) {
 #pragma unroll
-        for (int i = 0; i < C::kEpiCols / 2; ++i) {
-          const float2 o = xbuf[i * BM + row];
-          acc[i].x += o.x;
-          acc[i].y += o.y;
+          for (int i = 0; i < C::kEpiCols / 2; ++i) {
+            const float2 o = xbuf[i * C::kXRows + row];
+            acc[i].x += o.x;
+            acc[i].y += o.y;
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(xempty);
@@ -477,9 +493,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int BN>
+template <int BN, bool SMALL = false>
 constexpr uint32_t smem_bytes(int table_entries) {
-  return Cfg<BN>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
+  return Cfg<BN, SMALL>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
 }
 
 constexpr int kMaxExperts = 2048;
@@ -487,11 +503,13 @@ constexpr uint32_t kSmemLimit = 232448;  // 227 KB: the per-block dynamic shared
 static_assert(Cfg<256>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
 
 template <int BN, int MODE>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
-                  const CUtensorMap& tSA, const CUtensorMap& tD, int grid, int table_entries,
+                  const CUtensorMap& tD, int grid, int table_entries,
                   cudaStream_t stream) {
+  using C = Cfg<BN, MODE == kDenseSmallM>;
   auto kern = fp8_gemm_kernel<BN, MODE>;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
   int dev = 0;
@@ -499,11 +517,11 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN>(kMaxExperts + 1))) != cudaSuccess) {
+                             static_cast<int>(kSmemLimit)) != cudaSuccess) {
       cudaGetLastError();
       return FP8G_ERR_CUDA;
     }
-    if constexpr (Cfg<BN>::kRebalance) {
+    if constexpr (C::kRebalance) {
       // setmaxnreg.inc waits until the registers it asks for are free: the launch must hold
       // at least what the rebalanced warpgroups use, or the epilogue would never start.
       cudaFuncAttributes fa{};
@@ -511,13 +529,14 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
         cudaGetLastError();
         return FP8G_ERR_CUDA;
       }
-      if (fa.numRegs * Cfg<BN>::kThreads < 128 * static_cast<int>(Cfg<BN>::kRegsLow) +
-                                               256 * static_cast<int>(Cfg<BN>::kRegsHigh))
+      if (fa.numRegs * C::kThreads < 128 * static_cast<int>(C::kRegsLow) +
+                                         256 * static_cast<int>(C::kRegsHigh))
         return FP8G_ERR_CUDA;
     }
     attr_set.fetch_or(bit);
   }
-  kern<<<grid, Cfg<BN>::kThreads, smem_bytes<BN>(table_entries), stream>>>(tA, tB, tSA, tD, args);
+  kern<<<grid, C::kThreads, smem_bytes<BN, MODE == kDenseSmallM>(table_entries), stream>>>(tA, tB, tD,
+                                                                                          args);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
@@ -571,6 +590,8 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
 
   const int64_t m_blocks = (MODE == kMasked) ? o.E * ((o.cap + BM - 1) / BM) : (o.rows + BM - 1) / BM;
   const int bn = choose_block_n(m_blocks, o.N, dev->sm_count);
+  // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
+  const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
 
   GemmArgs a{};
   a.rows = static_cast<int32_t>(o.rows);
@@ -582,6 +603,8 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
   a.num_m = static_cast<int32_t>((o.rows + BM - 1) / BM);
   a.num_n = static_cast<int32_t>((o.N + bn - 1) / bn);
   a.num_tiles = a.num_m * a.num_n;
+  a.sA = o.sA;
+  a.ld_sa = o.ld_sa;
   a.sB = o.sB;
   a.D = static_cast<__nv_bfloat16*>(o.D);
   a.ldd = o.ldd;
@@ -589,11 +612,11 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
   a.status = dev->status;
   a.budget = wait_budget_cycles();
 
-  CUtensorMap tA, tB, tSA, tD;
+  CUtensorMap tA, tB, tD;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(o.K), static_cast<uint64_t>(o.rows)};
     const uint64_t strides[1] = {static_cast<uint64_t>(o.lda)};
-    const uint32_t box[2] = {BK, BM};
+    const uint32_t box[2] = {BK, small_m ? 64u : static_cast<uint32_t>(BM)};
     if ((st = encode_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, o.A, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
       return st;
@@ -605,14 +628,6 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
     const uint32_t box[3] = {BK, static_cast<uint32_t>(bn), 1};
     if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, o.B, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
-      return st;
-  }
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(o.rows), static_cast<uint64_t>(o.K / BK)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(o.ld_sa * 4)};
-    const uint32_t box[2] = {BM, 1};
-    if ((st = encode_tmap(&tSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, o.sA, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_NONE)) != FP8G_OK)
       return st;
   }
   {
@@ -633,13 +648,19 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
   switch (bn) {
     case 256:
       t_last_stages = Cfg<256>::kStages;
-      return launch_kernel<256, MODE>(a, tA, tB, tSA, tD, grid, table_entries, stream);
+      return launch_kernel<256, MODE>(a, tA, tB, tD, grid, table_entries, stream);
     case 128:
       t_last_stages = Cfg<128>::kStages;
-      return launch_kernel<128, MODE>(a, tA, tB, tSA, tD, grid, table_entries, stream);
+      return launch_kernel<128, MODE>(a, tA, tB, tD, grid, table_entries, stream);
     default:
+      if constexpr (MODE == kDense) {
+        if (small_m) {
+          t_last_stages = Cfg<64, true>::kStages;
+          return launch_kernel<64, kDenseSmallM>(a, tA, tB, tD, grid, table_entries, stream);
+        }
+      }
       t_last_stages = Cfg<64>::kStages;
-      return launch_kernel<64, MODE>(a, tA, tB, tSA, tD, grid, table_entries, stream);
+      return launch_kernel<64, MODE>(a, tA, tB, tD, grid, table_entries, stream);
   }
 }
 

@@ -39,47 +39,45 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
 
 // The e4m3 codes of the IEEE quotients x / s, without a division for almost every element.
 //
-// y = RN(x * r) with r = RN(1/s) differs from the exact quotient q by less than 2^-23 |q|,
-// so y and RN(q) are less than 3 ulps apart.  In e4m3's normal range (|y| >= 2^-6) the
-// rounding keeps 3 mantissa bits, and its decision points (the midpoints between
-// neighbouring codes) are the fp32 values whose low 20 mantissa bits are 0x80000.  When y
-// is more than 8 ulps from such a point, y and RN(q) round to the same code.  Elements
-// closer than that, and those below 2^-6 (where the code spacing is a fixed 2^-9), take
-// the IEEE division; so does everything when s is not a normal number (r inexact).
-__device__ __forceinline__ bool near_boundary(float y) {
-  const uint32_t u = __float_as_uint(y) & 0x7FFFFFFFu;
-  const bool small = (u - 1u) < 0x3C7FFFFFu;          // 0 < |y| < 2^-6
-  const bool mid = ((u & 0xFFFFFu) - 0x7FFF8u) < 17u;  // low 20 bits within 8 of 0x80000
-  return small || mid;
-}
-
-// N values / s -> N e4m3 codes, little-endian (value 0 in the lowest byte of w[0]).
+// With r = RN(1/s), the products y_lo = RN(x * RN(r (1 - 2^-20))) and y_hi = RN(x * RN(r (1 + 2^-20)))
+// differ from the exact quotient q by a relative factor 1 -+ 2^-20 up to rounding errors below
+// 3 * 2^-24, so RN(q) lies strictly between them.  Rounding to e4m3 (nearest-even, saturating)
+// is monotone, so when y_lo and y_hi give the same code, that is the code of RN(q).  Only the
+// pairs where the two differ (an e4m3 decision point within 2^-20 of q, about one element in
+// 2^16) take the IEEE division; so does every element when s is not a normal number (r would
+// be inexact).
 template <int N>
 __device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (&w)[N / 4]) {
+  static_assert(N % 4 == 0, "N");
   if (s == 0.0f) {
 #pragma unroll
     for (int i = 0; i < N / 4; ++i) w[i] = 0u;
     return;
   }
-  const float r = __frcp_rn(s);
-  const bool exact_all = !(s >= 1.17549435e-38f);  // subnormal s: divide every element
-  float y[N];
-  uint32_t redo = 0;
+  uint16_t c[N / 2];
+  if (s >= 1.17549435e-38f) {
+    const float r = __frcp_rn(s);
+    const float2 rlo = make_float2(__fmul_rn(r, 1.0f - 0x1p-20f), __fmul_rn(r, 1.0f - 0x1p-20f));
+    const float2 rhi = make_float2(__fmul_rn(r, 1.0f + 0x1p-20f), __fmul_rn(r, 1.0f + 0x1p-20f));
+    uint32_t redo = 0;
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    y[i] = __fmul_rn(f[i], r);
-    redo |= (exact_all || near_boundary(y[i])) ? (1u << i) : 0u;
-  }
-  if (redo != 0u) {  // rare: the IEEE division decides these elements
+    for (int i = 0; i < N / 2; ++i) {
+      const float2 x2 = make_float2(f[2 * i], f[2 * i + 1]);
+      const float2 lo = __fmul2_rn(x2, rlo), hi = __fmul2_rn(x2, rhi);
+      c[i] = cvt_e4m3x2(lo.y, lo.x);
+      redo |= (c[i] != cvt_e4m3x2(hi.y, hi.x)) ? (1u << i) : 0u;
+    }
+    if (redo != 0u) {  // rare: the IEEE division decides these pairs
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-      if (redo & (1u << i)) y[i] = __fdiv_rn(f[i], s);
+      for (int i = 0; i < N / 2; ++i)
+        if (redo & (1u << i)) c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i + 1], s), __fdiv_rn(f[2 * i], s));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i + 1], s), __fdiv_rn(f[2 * i], s));
   }
 #pragma unroll
-  for (int i = 0; i < N / 4; ++i) {
-    const uint16_t lo = cvt_e4m3x2(y[4 * i + 1], y[4 * i]), hi = cvt_e4m3x2(y[4 * i + 3], y[4 * i + 2]);
-    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
+  for (int i = 0; i < N / 4; ++i) w[i] = static_cast<uint32_t>(c[2 * i]) | (static_cast<uint32_t>(c[2 * i + 1]) << 16);
 }
 
 __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
