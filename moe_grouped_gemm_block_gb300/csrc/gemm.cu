@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
   auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + NB + b); };
   const uint32_t xfull = bar0 + 8u * (2 * S + 2 * NB);  // K-split exchange written
   const uint32_t xempty = xfull + 8u;                             // K-split exchange read
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);  // [0] tmem base, [1] abort
+  // misc: [0] TMEM base, [1] abort flag, [2] group table out of contract
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   int32_t* table = reinterpret_cast<int32_t*>(smem + C::kOffTable);
 
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             mma_f8f6f4_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-          mma_commit_if(leader, empty(s));
+          // one commit per K block: the epilogue, on seeing the partial, also frees the stage
           mma_commit_if(leader, tfull(b));
         }
       }
@@ -345,6 +346,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
     const int kpart = grp / C::kColGroups;                 // promotes K blocks kb % kKSplit == kpart
     const int col0 = (grp % C::kColGroups) * C::kEpiCols;  // column offset inside the tile
     const int row = q * 32 + lane;       // tile row owned by this thread
+    // one lane per K part frees the operand stage of each K block once its MMAs are done
+    const bool stage_releaser = lane == 0 && ew == kpart * 4 * C::kColGroups;
     const uint32_t out_addr = base + C::kOffOut + (ew % C::kStoreWarps) * C::kOutBytes;
     float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
     uint32_t it_base = 0, tiles_done = 0;
@@ -396,6 +399,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
         const float scale = sa_kb * sb_kb;
         const float2 scale2 = make_float2(scale, scale);
         if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
+        // the MMAs of this K block are complete: its operand stage can be refilled
+        if (stage_releaser) mbar_arrive(empty(it % S));
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
         if (live) {
@@ -403,14 +408,20 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
           for (int c = 0; c < C::kEpiCols / 64; ++c) {
             float v[64];
             tmem_ld64_sync(taddr + c * 64, v);
+            if (c == C::kEpiCols / 64 - 1) {  // all of this warp's columns are in registers:
+              tc_fence_before();               // release the TMEM buffer before the last FMAs
+              __syncwarp();
+              if (lane == 0) mbar_arrive(tempty(b));
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
           }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(b));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty(b));
       }
       it_base += a.KB;
       if (!ok) break;

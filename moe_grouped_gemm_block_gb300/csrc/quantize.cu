@@ -42,10 +42,22 @@ __device__ __forceinline__ float amax8(const float (&f)[8]) {
 // With r = RN(1/s), the products y_lo = RN(x * RN(r (1 - 2^-20))) and y_hi = RN(x * RN(r (1 + 2^-20)))
 // differ from the exact quotient q by a relative factor 1 -+ 2^-20 up to rounding errors below
 // 3 * 2^-24, so RN(q) lies strictly between them.  Rounding to e4m3 (nearest-even, saturating)
-// is monotone, so when y_lo and y_hi give the same code, that is the code of RN(q).  Only the
-// pairs where the two differ (an e4m3 decision point within 2^-20 of q, about one element in
-// 2^16) take the IEEE division; so does every element when s is not a normal number (r would
-// be inexact).
+// is monotone, so when y_lo and y_hi give the same code, that is the code of RN(q).  When any
+// element of a group disagrees (an e4m3 decision point within 2^-20 of its quotient, about one
+// element in 2^16), the whole group takes the IEEE division; so does every element when s is
+// not a normal number (r would be inexact).
+// Four values -> four e4m3 codes packed in one word (value 0 in the lowest byte).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(w)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return w;
+}
+
 template <int N>
 __device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (&w)[N / 4]) {
   static_assert(N % 4 == 0, "N");
@@ -54,30 +66,28 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (
     for (int i = 0; i < N / 4; ++i) w[i] = 0u;
     return;
   }
-  uint16_t c[N / 2];
-  if (s >= 1.17549435e-38f) {
+  bool exact = !(s >= 1.17549435e-38f);  // subnormal s: divide every element
+  if (!exact) {
     const float r = __frcp_rn(s);
-    const float2 rlo = make_float2(__fmul_rn(r, 1.0f - 0x1p-20f), __fmul_rn(r, 1.0f - 0x1p-20f));
-    const float2 rhi = make_float2(__fmul_rn(r, 1.0f + 0x1p-20f), __fmul_rn(r, 1.0f + 0x1p-20f));
-    uint32_t redo = 0;
+    const float lo_f = __fmul_rn(r, 1.0f - 0x1p-20f), hi_f = __fmul_rn(r, 1.0f + 0x1p-20f);
+    const float2 rlo = make_float2(lo_f, lo_f), rhi = make_float2(hi_f, hi_f);
+    uint32_t diff = 0;
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-      const float2 x2 = make_float2(f[2 * i], f[2 * i + 1]);
-      const float2 lo = __fmul2_rn(x2, rlo), hi = __fmul2_rn(x2, rhi);
-      c[i] = cvt_e4m3x2(lo.y, lo.x);
-      redo |= (c[i] != cvt_e4m3x2(hi.y, hi.x)) ? (1u << i) : 0u;
+    for (int i = 0; i < N / 4; ++i) {
+      const float2 x01 = make_float2(f[4 * i], f[4 * i + 1]), x23 = make_float2(f[4 * i + 2], f[4 * i + 3]);
+      const float2 l01 = __fmul2_rn(x01, rlo), l23 = __fmul2_rn(x23, rlo);
+      const float2 h01 = __fmul2_rn(x01, rhi), h23 = __fmul2_rn(x23, rhi);
+      w[i] = cvt_e4m3x4(l01.x, l01.y, l23.x, l23.y);
+      diff |= w[i] ^ cvt_e4m3x4(h01.x, h01.y, h23.x, h23.y);
     }
-    if (redo != 0u) {  // rare: the IEEE division decides these pairs
-#pragma unroll
-      for (int i = 0; i < N / 2; ++i)
-        if (redo & (1u << i)) c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i + 1], s), __fdiv_rn(f[2 * i], s));
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i + 1], s), __fdiv_rn(f[2 * i], s));
+    exact = diff != 0u;  // rare: some element sits within 2^-20 of a decision point
   }
+  if (exact) {
 #pragma unroll
-  for (int i = 0; i < N / 4; ++i) w[i] = static_cast<uint32_t>(c[2 * i]) | (static_cast<uint32_t>(c[2 * i + 1]) << 16);
+    for (int i = 0; i < N / 4; ++i)
+      w[i] = cvt_e4m3x4(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s), __fdiv_rn(f[4 * i + 2], s),
+                        __fdiv_rn(f[4 * i + 3], s));
+  }
 }
 
 __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
