@@ -47,7 +47,9 @@ constexpr int BK = 128;  // K per stage = the scaling block
 constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a band)
 constexpr int kSAAhead = 4;  // K-block steps by which the A-row scales are loaded ahead
 
-template <int BN, bool SMALL = false>
+// PAIR: a cluster of two CTAs computes 256 x BN tiles with tcgen05.mma.cta_group::2; each CTA
+// loads its 128 A rows and half of the B tile (BN / 2 rows), so a stage is 32 KB and six fit.
+template <int BN, bool SMALL = false, bool PAIR = false>
 struct Cfg {
   static constexpr int kEpiCols = BN >= 128 ? 128 : BN;  // columns per epilogue warp
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
@@ -67,13 +69,14 @@ struct Cfg {
   // A rows loaded per stage: the MMA always reads 128 rows, and with SMALL the upper 64 are
   // whatever follows in shared memory (those rows of D are computed but never stored).
   static constexpr int kARows = SMALL ? 64 : BM;
-  static constexpr int kStages = SMALL ? 12 : (BN == 256 ? 4 : 6);
+  static constexpr int kStages = SMALL ? 12 : (PAIR ? 6 : (BN == 256 ? 4 : 6));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kABytes = kARows * BK;
-  static constexpr uint32_t kBBytes = BN * BK;
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows this CTA loads per stage
+  static constexpr uint32_t kBBytes = kBRows * BK;
   static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per store warp
   static constexpr int kXRows = SMALL ? 64 : BM;
   static constexpr uint32_t kXBytes = kKSplit > 1 ? kXRows * BN * 4 : 0;  // K-split exchange
@@ -89,6 +92,7 @@ struct Cfg {
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
+  static_assert(!PAIR || (BN == 256 && !SMALL), "CTA pairs use 256-wide tiles");
 };
 
 struct GemmArgs {
@@ -162,6 +166,51 @@ __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table
   }
 }
 
+// CTA-pair tile index -> this CTA's half (rank 0: the first 128 rows of the 256-row tile).
+// Every pair tile is computed by both CTAs; a half whose rows are all outside the matrix or
+// group has rows <= 0 and stores nothing.
+template <int BN, int MODE>
+__device__ __forceinline__ void get_pair_tile(const GemmArgs& a, const int32_t* table, const int32_t* ptab,
+                                              int32_t t, uint32_t rank, Tile& ti) {
+  if (MODE == kDense) {
+    constexpr int kBand = kBandM / 2;  // pairs per raster band
+    const int32_t num_mp = (a.num_m + 1) >> 1;
+    const int32_t band_tiles = kBand * a.num_n;
+    const int32_t band = t / band_tiles, r = t - band * band_tiles;
+    const int32_t p_first = band * kBand;
+    const int32_t gm = min(kBand, num_mp - p_first);
+    const int32_t mp = p_first + r % gm, nb = r / gm;
+    ti.a_row = (2 * mp + static_cast<int32_t>(rank)) * BM;
+    ti.n0 = nb * BN;
+    ti.rows = min(BM, a.rows - ti.a_row);
+    ti.g = 0;
+    return;
+  }
+  // grouped: ptab[e] = pair tiles (per column block) of experts < e; pairs m-block fastest
+  int lo = 0, hi = a.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<int64_t>(ptab[mid]) * a.num_n <= t) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int32_t pairs = ptab[e + 1] - ptab[e];
+  const int32_t local = t - ptab[e] * a.num_n;
+  const int32_t pr = local % pairs, nb = local / pairs;
+  const int32_t mb = 2 * pr + static_cast<int32_t>(rank);  // m-block of this CTA within the expert
+  ti.g = e;
+  ti.n0 = nb * BN;
+  if (MODE == kContiguous) {
+    const int32_t first = table[e], end = table[e + 1];
+    ti.a_row = first + mb * BM;
+    ti.rows = ti.a_row < end ? BM : 0;
+  } else {
+    int32_t cnt = __ldg(a.groups + e);
+    cnt = min(max(cnt, 0), a.cap);
+    ti.a_row = e * a.cap + mb * BM;
+    ti.rows = min(BM, cnt - mb * BM);
+  }
+}
+
 // Bounded wait on an mbarrier phase.  On timeout: flag the CTA, record the status.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmArgs& a,
                                              volatile int* abort_flag) {
@@ -178,12 +227,12 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   return true;
 }
 
-template <int BN, int MODE>
-__global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
+template <int BN, int MODE, bool PAIR = false>
+__global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD,
                     const GemmArgs a) {
-  using C = Cfg<BN, MODE == kDenseSmallM>;
+  using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_u32(smem);
@@ -192,6 +241,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // rank 0 of a pair issues the MMAs
   const uint32_t bar0 = base + C::kOffBar;
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty = [&](uint32_t s) { return bar0 + 8u * (S + s); };
@@ -213,7 +263,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
     // each TMEM buffer is consumed by the warps of one K part
     for (uint32_t b = 0; b < NB; ++b) {
       mbar_init(tfull(b), 1);
-      mbar_init(tempty(b), C::kStoreWarps);
+      // in a pair, the promotion warps of both CTAs release rank 0's buffer
+      mbar_init(tempty(b), PAIR ? 2 * C::kStoreWarps : C::kStoreWarps);
     }
     mbar_init(xfull, C::kStoreWarps);
     mbar_init(xempty, C::kStoreWarps);
@@ -225,9 +276,16 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
     prefetch_tmap(&tmD);
   }
   if (warp == 1) {
-    tmem_alloc(base + C::kOffMisc, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {  // one warp of each CTA of the pair, collectively
+      tmem_alloc_pair(base + C::kOffMisc, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(base + C::kOffMisc, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
+  // pair tiles per expert (prefix over experts), after the group table
+  int32_t* ptab = table + (a.E + 1);
   // Group tables (grouped modes), built by the first epilogue warp.
   if (MODE == kContiguous && warp == C::kEpiWarp0) {
     bool bad = false;
@@ -241,11 +299,28 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
       misc[2] = 1;
       record_status(a.status, FP8G_ERR_DEVICE_ASSERT);
     }
+    if constexpr (PAIR) {
+      __syncwarp();
+      int32_t running = 0;
+      if (lane == 0) ptab[0] = 0;
+      for (int e0 = 0; e0 < a.E; e0 += 32) {
+        const int e = e0 + lane;
+        int32_t prs = 0;
+        if (e < a.E) prs = (max(table[e + 1] - table[e], 0) / BM + 1) >> 1;
+        int32_t incl = prs;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        if (e < a.E) ptab[e + 1] = running + incl;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
   }
   if (MODE == kMasked && warp == C::kEpiWarp0) {
     int32_t running = 0;
     bool bad = false;
-    if (lane == 0) table[0] = 0;
     for (int e0 = 0; e0 < a.E; e0 += 32) {
       const int e = e0 + lane;
       int32_t mbs = 0;
@@ -254,6 +329,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
         if (cnt < 0 || cnt > a.cap) bad = true;
         const int32_t c = min(max(cnt, 0), a.cap);
         mbs = (c + BM - 1) / BM;
+        if (PAIR) mbs = (mbs + 1) >> 1;  // pair tiles
       }
       int32_t incl = mbs;
 #pragma unroll
@@ -261,18 +337,32 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
         const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += v;
       }
-      if (e < a.E) table[e + 1] = running + incl;
+      if (e < a.E) (PAIR ? ptab : table)[e + 1] = running + incl;
       running += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) (PAIR ? ptab : table)[0] = 0;
     if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(a.status, FP8G_ERR_DEVICE_ASSERT);
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers and TMEM exist before any signalling
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
 
   int32_t num_tiles = a.num_tiles;
-  if (MODE == kMasked) num_tiles = table[a.E] * a.num_n;
+  if (MODE == kMasked) num_tiles = (PAIR ? ptab : table)[a.E] * a.num_n;
+  if (PAIR && MODE == kContiguous) num_tiles = ptab[a.E] * a.num_n;
+  // a CTA pair walks the tiles of its cluster index; both CTAs see every pair tile
+  const int32_t tile0 = PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
+  const int32_t tile_step = PAIR ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
+  auto fetch_tile = [&](int32_t t, Tile& ti) -> bool {
+    if constexpr (PAIR) {
+      get_pair_tile<BN, MODE>(a, table, ptab, t, rank, ti);
+      return true;
+    } else {
+      return get_tile<BN, MODE>(a, table, t, ti);
+    }
+  };
   if (MODE == kContiguous && misc[2]) num_tiles = 0;
   if (warp < C::kEpiWarp0) {
     if constexpr (C::kRebalance) regs_release<C::kRegsLow>();
@@ -283,18 +373,27 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       uint32_t it = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
         Tile ti;
-        if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
+        if (!fetch_tile(t, ti)) continue;
         for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           if (!__all_sync(0xffffffffu, wait_bounded(empty(s), ph ^ 1u, a, abort_flag))) { ok = false; break; }
-          mbar_arrive_expect_tx_if(leader, full(s), C::kABytes + C::kBBytes);
-          tma_load_2d_if(leader, base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
-          tma_load_3d_if(leader, base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on rank 0's full barrier, which expects the pair's bytes
+            const uint32_t fb = mapa_shared(full(s), 0);
+            mbar_arrive_expect_tx_if(leader && rank == 0, full(s), 2 * (C::kABytes + C::kBBytes));
+            tma_load_2d_pair_if(leader, base + C::kOffA + s * C::kABytes, &tmA, fb, kb * BK, ti.a_row);
+            tma_load_3d_pair_if(leader, base + C::kOffB + s * C::kBBytes, &tmB, fb, kb * BK,
+                                ti.n0 + static_cast<int32_t>(rank) * C::kBRows, ti.g);
+          } else {
+            mbar_arrive_expect_tx_if(leader, full(s), C::kABytes + C::kBBytes);
+            tma_load_2d_if(leader, base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
+            tma_load_3d_if(leader, base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
+          }
         }
       }
-      if (!ok && leader) {  // let the loads already issued land before the CTA exits
+      if (!ok && leader && rank == 0) {  // let the loads already issued land before the CTA exits
         const uint32_t n = it < S ? it : S;
         for (uint32_t i = it - n; i < it; ++i) {
           const long long t0 = clock64();
@@ -302,18 +401,18 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
           }
         }
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+    } else if (warp == 1 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer (rank 0 of a pair)
+      constexpr uint32_t idesc = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
       // descriptors of stage 0; stage s and K step k add (offset in bytes) / 16 to the
       // 14-bit start-address field (shared addresses stay below 2^18, so it cannot carry)
       const uint64_t adesc0 = smem_desc_k_sw128(base + C::kOffA);
       const uint64_t bdesc0 = smem_desc_k_sw128(base + C::kOffB);
       uint32_t it = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
         Tile ti;
-        if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
+        if (!fetch_tile(t, ti)) continue;
         for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           const uint32_t b = it % NB, tph = (it / NB) & 1u;
@@ -323,11 +422,19 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
           const uint64_t ad = adesc0 + ((s * C::kABytes) >> 4);
           const uint64_t bd = bdesc0 + ((s * C::kBBytes) >> 4);
           const uint32_t d_tmem = tmem_base + b * BN;
+          if constexpr (PAIR) {
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_f8f6f4_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-          // one commit per K block: the epilogue, on seeing the partial, also frees the stage
-          mma_commit_if(leader, tfull(b));
+            for (int k = 0; k < BK / 32; ++k)
+              mma_f8f6f4_pair_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+            mma_commit_pair_if(leader, empty(s), 0x3);  // both CTAs' stage s is free
+            mma_commit_pair_if(leader, tfull(b), 0x3);  // both CTAs' partial is ready
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              mma_f8f6f4_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+            // one commit per K block: the epilogue, on seeing the partial, also frees the stage
+            mma_commit_if(leader, tfull(b));
+          }
         }
       }
       if (!ok && it > 0 && leader) {  // wait for the MMAs already issued before TMEM is released
@@ -347,18 +454,25 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
     const int col0 = (grp % C::kColGroups) * C::kEpiCols;  // column offset inside the tile
     const int row = q * 32 + lane;       // tile row owned by this thread
     // one lane per K part frees the operand stage of each K block once its MMAs are done
-    const bool stage_releaser = lane == 0 && ew == kpart * 4 * C::kColGroups;
+    const bool stage_releaser = !PAIR && lane == 0 && ew == kpart * 4 * C::kColGroups;
+    // this warp's TMEM buffers are released on rank 0's barrier (its own CTA unless paired)
+    auto release_tmem = [&](uint32_t b) {
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty(b), 0));
+        else mbar_arrive(tempty(b));
+      }
+    };
     const uint32_t out_addr = base + C::kOffOut + (ew % C::kStoreWarps) * C::kOutBytes;
     float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
     uint32_t it_base = 0, tiles_done = 0;
     bool ok = true;
-    for (int32_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
       Tile ti;
-      if (!get_tile<BN, MODE>(a, table, t, ti)) continue;
+      if (!fetch_tile(t, ti)) continue;
       const int32_t ncol0 = ti.n0 + col0;
       const bool has_cols = ncol0 < a.N;
       // small-M tiles: warps whose rows are all past M skip the promotion (nothing to store)
-      const bool live = MODE != kDenseSmallM || q * 32 < ti.rows;
+      const bool live = (MODE != kDenseSmallM && !PAIR) || q * 32 < ti.rows;
       const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
       // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
       // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
@@ -411,7 +525,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
             if (c == C::kEpiCols / 64 - 1) {  // all of this warp's columns are in registers:
               tc_fence_before();               // release the TMEM buffer before the last FMAs
               __syncwarp();
-              if (lane == 0) mbar_arrive(tempty(b));
+              release_tmem(b);
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -420,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
         } else {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty(b));
+          release_tmem(b);
         }
       }
       it_base += a.KB;
@@ -498,15 +612,19 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool SMALL = false>
+template <int BN, bool SMALL = false, bool PAIR = false>
 constexpr uint32_t smem_bytes(int table_entries) {
-  return Cfg<BN, SMALL>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
+  return Cfg<BN, SMALL, PAIR>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
 }
 
 constexpr int kMaxExperts = 2048;
@@ -515,13 +633,14 @@ static_assert(Cfg<256>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem")
 static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
+static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool PAIR = false>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
                   const CUtensorMap& tD, int grid, int table_entries,
                   cudaStream_t stream) {
-  using C = Cfg<BN, MODE == kDenseSmallM>;
-  auto kern = fp8_gemm_kernel<BN, MODE>;
+  using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
+  auto kern = fp8_gemm_kernel<BN, MODE, PAIR>;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -546,12 +665,39 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     }
     attr_set.fetch_or(bit);
   }
-  kern<<<grid, C::kThreads, smem_bytes<BN, MODE == kDenseSmallM>(table_entries), stream>>>(tA, tB, tD,
-                                                                                          args);
+  const uint32_t smem = smem_bytes<BN, MODE == kDenseSmallM, PAIR>(table_entries);
+  if constexpr (PAIR) {  // clusters of two CTAs (the grid is even)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, args) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8G_ERR_CUDA;
+    }
+    return FP8G_OK;
+  }
+  kern<<<grid, C::kThreads, smem, stream>>>(tA, tB, tD, args);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
 thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0;
+
+// FP8G_PAIR=1 runs 256-wide tiles on CTA pairs.  Off by default: with two TMEM partial
+// buffers per CTA, the pair's cross-CTA hops lengthen the MMA / promotion hand-off more than the
+// deeper ring gains (measured ~10% slower on 4096 x 8192 x 8192).
+bool env_pair() {
+  const char* e = std::getenv("FP8G_PAIR");
+  return e && e[0] == '1';
+}
 
 // FP8G_BLOCK_N (64, 128 or 256) forces the tile width; read on every call.
 int env_block_n() {
@@ -603,6 +749,9 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
   const int bn = choose_block_n(m_blocks, o.N, dev->sm_count);
   // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
   const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
+  // 256-wide tiles run as CTA pairs (256 x 256 per pair) unless there are too few rows
+  const bool pair = bn == 256 && env_pair() &&
+                    (MODE != kDense || (o.rows + BM - 1) / BM >= 2) && dev->sm_count >= 2;
 
   GemmArgs a{};
   a.rows = static_cast<int32_t>(o.rows);
@@ -636,7 +785,7 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
     const uint64_t dims[3] = {static_cast<uint64_t>(o.K), static_cast<uint64_t>(o.N),
                               static_cast<uint64_t>(o.E)};
     const uint64_t strides[2] = {static_cast<uint64_t>(o.ldb), static_cast<uint64_t>(o.ldb * o.N)};
-    const uint32_t box[3] = {BK, static_cast<uint32_t>(bn), 1};
+    const uint32_t box[3] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn), 1};
     if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, o.B, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
       return st;
@@ -652,12 +801,24 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
 
   int64_t tiles_upper = (MODE == kMasked) ? m_blocks * a.num_n : static_cast<int64_t>(a.num_tiles);
   int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(tiles_upper, 1), dev->sm_count));
-  const int table_entries = (MODE == kDense) ? 0 : static_cast<int>(o.E + 1);
+  int table_entries = (MODE == kDense) ? 0 : static_cast<int>(o.E + 1);
+  if (pair) {
+    // pair tiles: dense ceil(num_m/2) x num_n; grouped at most (m-blocks + experts)/2 x num_n
+    if (MODE == kDense) a.num_tiles = ((a.num_m + 1) / 2) * a.num_n;
+    const int64_t pair_upper = (MODE == kDense) ? a.num_tiles : ((m_blocks + o.E + 1) / 2) * a.num_n;
+    grid = 2 * static_cast<int>(std::min<int64_t>(std::max<int64_t>(pair_upper, 1), dev->sm_count / 2));
+    if (MODE != kDense) table_entries = 2 * static_cast<int>(o.E + 1);
+  }
 
   t_last_bn = bn;
   t_last_grid = grid;
   switch (bn) {
     case 256:
+      if (pair) {
+        t_last_stages = Cfg<256, false, true>::kStages;
+        return launch_kernel<256, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
+                                                                               table_entries, stream);
+      }
       t_last_stages = Cfg<256>::kStages;
       return launch_kernel<256, MODE>(a, tA, tB, tD, grid, table_entries, stream);
     case 128:

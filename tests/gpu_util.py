@@ -70,24 +70,34 @@ def assert_gemm_close(gpu: np.ndarray, ref_bits: np.ndarray, what: str = ""):
     return {"max_abs": float(err.max(initial=0)), "fro": float(fro), "exact": float(np.mean(err == 0))}
 
 
-class block_n:
-    """Force the tile width of the GEMM calls inside the block (FP8G_BLOCK_N)."""
+class env_var:
+    """Set (or, with None, clear) one environment variable inside the block."""
 
-    def __init__(self, bn):
-        self.bn = bn
+    def __init__(self, name, value):
+        self.name, self.value = name, value
 
     def __enter__(self):
-        self.old = os.environ.get("FP8G_BLOCK_N")
-        if self.bn:
-            os.environ["FP8G_BLOCK_N"] = str(self.bn)
+        self.old = os.environ.get(self.name)
+        if self.value is None:
+            os.environ.pop(self.name, None)
         else:
-            os.environ.pop("FP8G_BLOCK_N", None)
+            os.environ[self.name] = str(self.value)
 
     def __exit__(self, *exc):
         if self.old is None:
-            os.environ.pop("FP8G_BLOCK_N", None)
+            os.environ.pop(self.name, None)
         else:
-            os.environ["FP8G_BLOCK_N"] = self.old
+            os.environ[self.name] = self.old
+
+
+def block_n(bn):
+    """Force the tile width of the GEMM calls inside the block (FP8G_BLOCK_N)."""
+    return env_var("FP8G_BLOCK_N", bn or None)
+
+
+def pair(on):
+    """Turn the CTA-pair kernel for 256-wide tiles on or off (FP8G_PAIR)."""
+    return env_var("FP8G_PAIR", 1 if on else None)
 
 
 def check_status():

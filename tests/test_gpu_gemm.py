@@ -15,7 +15,7 @@ import torch
 import moe_grouped_gemm_block_gb300 as g
 from moe_grouped_gemm_block_gb300.workloads import WORKLOADS, make_inputs, round_up
 from oracle import gemm_nt, grouped_contiguous, grouped_masked, quantize_128x128, quantize_1x128
-from tests.gpu_util import (assert_gemm_close, bf16_bits, bf16_to_np, block_n, check_status, need_gpu,
+from tests.gpu_util import (assert_gemm_close, bf16_bits, bf16_to_np, block_n, check_status, need_gpu, pair,
                             sa_from_device, sa_to_device, u8)
 
 pytestmark = pytest.mark.gpu
@@ -61,6 +61,17 @@ def test_dense_small_shapes(M, N, K, bn):
     qa, sa, qb, sb = _problem(M, N, K, seed=M * 7 + N + K)
     D = _dense_gpu(qa, sa, qb, sb, bn)
     assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} bn={bn}")
+
+
+@pytest.mark.parametrize("use_pair", [True, False])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (300, 272, 384), (640, 768, 1024), (129, 512, 256)])
+def test_dense_256_wide_single_cta_and_pair(M, N, K, use_pair):
+    qa, sa, qb, sb = _problem(M, N, K, seed=M + 3 * N + K)
+    with pair(use_pair):
+        D = _dense_gpu(qa, sa, qb, sb, 256)
+        cfg = g.fp8g_last_config()
+    assert cfg["block_n"] == 256 and (cfg["stages"] == 6) == (use_pair and M > 128)
+    assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} pair={use_pair}")
 
 
 def test_dense_strided_operands():
@@ -169,10 +180,11 @@ def _contig_gpu(qa, sa, qb, sb, offs, bn=None):
     return D
 
 
-@pytest.mark.parametrize("bn", [None, 256, 128, 64])
-def test_contiguous_small(bn):
+@pytest.mark.parametrize("bn,use_pair", [(None, True), (256, True), (256, False), (128, True), (64, True)])
+def test_contiguous_small(bn, use_pair):
     qa, sa, qb, sb, offs = _contig_problem([100, 0, 300, 128, 1], N=272, K=384, seed=5, extra_rows=128)
-    D = _contig_gpu(qa, sa, qb, sb, offs, bn)
+    with pair(use_pair):
+        D = _contig_gpu(qa, sa, qb, sb, offs, bn)
     check_status()
     init = np.full((qa.shape[0], qb.shape[1]), SENTINEL, np.uint16)
     ref = grouped_contiguous(qa, sa, qb, sb, offs, init)
@@ -243,12 +255,13 @@ def _masked_problem(E, cap, N, K, seed):
     return qa.reshape(E, cap, K), sa.reshape(E, cap, -1), np.stack(qbs), np.stack(sbs)
 
 
-@pytest.mark.parametrize("bn", [None, 256, 128, 64])
-def test_masked_small(bn):
+@pytest.mark.parametrize("bn,use_pair", [(None, True), (256, True), (256, False), (128, True), (64, True)])
+def test_masked_small(bn, use_pair):
     E, cap, N, K = 5, 160, 272, 384
     masked = [0, 1, 160, 37, 129]
     qa, sa, qb, sb = _masked_problem(E, cap, N, K, seed=21)
-    D = _masked_gpu(qa, sa, qb, sb, masked, bn)
+    with pair(use_pair):
+        D = _masked_gpu(qa, sa, qb, sb, masked, bn)
     check_status()
     ref = grouped_masked(qa, sa, qb, sb, masked, np.full((E, cap, N), SENTINEL, np.uint16))
     got = bf16_bits(D)
