@@ -59,31 +59,43 @@ struct Cfg {
   static constexpr int kEpiGroups = kColGroups * kKSplit;  // warpgroups of epilogue warps
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kStoreWarps = 4 * kColGroups;     // warps that write D
-  // BN = 256: three full warpgroups (producer / MMA / 2 idle, then 2 epilogue warpgroups) so
+  // MMA issuing threads (lane 0 of warps 1 .. kMmaWarps), taking alternate pipeline stages.
+  // One thread pays ~60 cycles per tcgen05.mma plus ~170 per mbarrier round trip, which caps
+  // the narrow small-M tiles (whose MMAs are short); there two issuers share the stream.
+  // Wider tiles keep one: their MMAs are long enough, and measured slower with two.
+  static constexpr int kMmaWarps = SMALL ? 2 : 1;
+  // BN = 256: three full warpgroups (producer / 2 MMA / idle, then 2 epilogue warpgroups) so
   // that setmaxnreg can move registers to the epilogue: the launch gives 384 x 168 = 64512,
-  // rebalanced to 128 x 40 + 256 x 232 = 64512.  Otherwise: 2 warps + 1 epilogue warpgroup.
-  static constexpr int kEpiWarp0 = BN == 256 ? 4 : 2;
+  // rebalanced to 128 x 40 + 256 x 232 = 64512.  Otherwise: producer and MMA warps, then the
+  // epilogue warpgroups (any four consecutive warps cover the four TMEM lane quarters).
+  static constexpr int kEpiWarp0 = BN == 256 ? 4 : 1 + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr bool kRebalance = BN == 256;
   static constexpr uint32_t kRegsLow = 40, kRegsHigh = 232;
   // A rows loaded per stage: the MMA always reads 128 rows, and with SMALL the upper 64 are
   // whatever follows in shared memory (those rows of D are computed but never stored).
   static constexpr int kARows = SMALL ? 64 : BM;
-  static constexpr int kStages = SMALL ? 12 : (PAIR ? 6 : (BN == 256 ? 4 : 6));
+  // K blocks per pipeline stage.  One TMA box then covers kKPS consecutive 128-byte pieces of
+  // every row (a kKPS * 128-byte run in global memory): streaming weights from HBM in 128-byte
+  // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
+  static constexpr int kKPS = SMALL ? 2 : 1;
+  static constexpr int kStages = SMALL ? 6 : (PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kABytes = kARows * BK;
-  static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows this CTA loads per stage
-  static constexpr uint32_t kBBytes = kBRows * BK;
+  static constexpr uint32_t kABytes = kARows * BK;       // one K block of A
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;      // B rows this CTA loads
+  static constexpr uint32_t kBBytes = kBRows * BK;       // one K block of B
+  static constexpr uint32_t kStageABytes = kKPS * kABytes;
+  static constexpr uint32_t kStageBBytes = kKPS * kBBytes;
   static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per store warp
   static constexpr int kXRows = SMALL ? 64 : BM;
   static constexpr uint32_t kXBytes = kKSplit > 1 ? kXRows * BN * 4 : 0;  // K-split exchange
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
-  static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-  static constexpr uint32_t kOffOut = kOffB + kStages * kBBytes;
+  static constexpr uint32_t kOffB = kOffA + kStages * kStageABytes;
+  static constexpr uint32_t kOffOut = kOffB + kStages * kStageBBytes;
   static constexpr uint32_t kOffX = kOffOut + kStoreWarps * kOutBytes;
   static constexpr uint32_t kOffBar = kOffX + kXBytes;
   static constexpr uint32_t kNumBars = 2 * kStages + 2 * kTmemBufs + 2;
@@ -92,7 +104,8 @@ struct Cfg {
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
-  static_assert(!PAIR || (BN == 256 && !SMALL), "CTA pairs use 256-wide tiles");
+  static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
+  static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
 };
 
 struct GemmArgs {
@@ -227,6 +240,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   return true;
 }
 
+// Wait for a phase that an earlier mbar_test_wait may already have seen complete (`seen`).  A
+// lone issuing thread pays the full round trip of every mbarrier test (~170 cycles, complete or
+// not), so the producer and MMA loops start the test for their next wait before issuing the
+// current copies / MMAs, and consume the result here.  A phase seen complete stays complete:
+// the barrier's next phase needs this thread's own work first.
+__device__ __forceinline__ bool wait_seen(bool seen, uint32_t bar, uint32_t parity, const GemmArgs& a,
+                                          volatile int* abort_flag) {
+  return seen || wait_bounded(bar, parity, a, abort_flag);
+}
+
 template <int BN, int MODE, bool PAIR = false>
 __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -246,6 +269,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   auto full = [&](uint32_t s) { return bar0 + 8u * s; };
   auto empty = [&](uint32_t s) { return bar0 + 8u * (S + s); };
   constexpr uint32_t NB = C::kTmemBufs;
+  // TMEM buffer b: partial written (tfull) / read (tempty)
   auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
   auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + NB + b); };
   const uint32_t xfull = bar0 + 8u * (2 * S + 2 * NB);  // K-split exchange written
@@ -258,7 +282,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), 1);  // the commit of the stage's issuer
     }
     // each TMEM buffer is consumed by the warps of one K part
     for (uint32_t b = 0; b < NB; ++b) {
@@ -366,30 +390,50 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   if (MODE == kContiguous && misc[2]) num_tiles = 0;
   if (warp < C::kEpiWarp0) {
     if constexpr (C::kRebalance) regs_release<C::kRegsLow>();
-    // Producer and MMA warps: all 32 lanes run the loop (warp-uniform control flow and
-    // operands); lane 0 alone issues the TMA copies, the MMAs and the commits.
     const bool leader = lane == 0;
-    if (warp == 0) {
+    constexpr int KPS = C::kKPS;
+    constexpr int MW = C::kMmaWarps;
+    // One issuer (wide tiles): the producer and MMA warps run their loops with all 32 lanes
+    // (warp-uniform control flow and operands), lane 0 issuing; the epilogue frees each stage
+    // when it sees the stage's partial.  Two issuers (small-M tiles): lane 0 alone runs each
+    // loop, tests its next barriers ahead (wait_seen) and frees stages by an MMA commit.  Each
+    // form measured faster where it is used.
+    constexpr bool kLone = MW > 1;
+    static_assert(KPS == 1 || kLone, "multi-K-block stages are freed by the issuers' commits");
+    static_assert(!kLone || !PAIR, "CTA pairs have one issuer");
+    // the tensor maps view A as [K/128][rows][128] and B as [E][K/128][N][128] (outer to
+    // inner), so one box holds KPS K blocks of the tile's rows, K block by K block
+    if (warp == 0 && (!kLone || leader)) {
       // ---------------------------------------------------------- TMA producer
-      uint32_t it = 0;
+      uint32_t it = 0;  // stages filled
       bool ok = true;
+      bool empty_seen = false;  // early test of the next stage's empty barrier (lone form)
       for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
         Tile ti;
         if (!fetch_tile(t, ti)) continue;
-        for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
+        // the K blocks of a stage past the end of K are zero-filled and never read
+        for (int32_t kb = 0; kb < a.KB; kb += KPS, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!__all_sync(0xffffffffu, wait_bounded(empty(s), ph ^ 1u, a, abort_flag))) { ok = false; break; }
+          bool ready;
+          if constexpr (kLone) {
+            ready = wait_seen(empty_seen, empty(s), ph ^ 1u, a, abort_flag);
+            empty_seen = mbar_test_wait(empty((it + 1) % S), (((it + 1) / S) & 1u) ^ 1u);
+          } else {
+            ready = __all_sync(0xffffffffu, wait_bounded(empty(s), ph ^ 1u, a, abort_flag));
+          }
+          if (!ready) { ok = false; break; }
+          const uint32_t dA = base + C::kOffA + s * C::kStageABytes;
+          const uint32_t dB = base + C::kOffB + s * C::kStageBBytes;
           if constexpr (PAIR) {
             // both CTAs' copies complete on rank 0's full barrier, which expects the pair's bytes
             const uint32_t fb = mapa_shared(full(s), 0);
-            mbar_arrive_expect_tx_if(leader && rank == 0, full(s), 2 * (C::kABytes + C::kBBytes));
-            tma_load_2d_pair_if(leader, base + C::kOffA + s * C::kABytes, &tmA, fb, kb * BK, ti.a_row);
-            tma_load_3d_pair_if(leader, base + C::kOffB + s * C::kBBytes, &tmB, fb, kb * BK,
-                                ti.n0 + static_cast<int32_t>(rank) * C::kBRows, ti.g);
+            mbar_arrive_expect_tx(leader && rank == 0, full(s), 2 * (C::kStageABytes + C::kStageBBytes));
+            tma_load_3d_pair(leader, dA, &tmA, fb, 0, ti.a_row, kb);
+            tma_load_4d_pair(leader, dB, &tmB, fb, 0, ti.n0 + static_cast<int32_t>(rank) * C::kBRows, kb, ti.g);
           } else {
-            mbar_arrive_expect_tx_if(leader, full(s), C::kABytes + C::kBBytes);
-            tma_load_2d_if(leader, base + C::kOffA + s * C::kABytes, &tmA, full(s), kb * BK, ti.a_row);
-            tma_load_3d_if(leader, base + C::kOffB + s * C::kBBytes, &tmB, full(s), kb * BK, ti.n0, ti.g);
+            mbar_arrive_expect_tx(leader, full(s), C::kStageABytes + C::kStageBBytes);
+            tma_load_3d(leader, dA, &tmA, full(s), 0, ti.a_row, kb);
+            tma_load_4d(leader, dB, &tmB, full(s), 0, ti.n0, kb, ti.g);
           }
         }
       }
@@ -401,49 +445,109 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
           }
         }
       }
-    } else if (warp == 1 && rank == 0) {
-      // ---------------------------------------------------------- MMA issuer (rank 0 of a pair)
+    } else if (warp >= 1 && warp <= MW && rank == 0 && (!kLone || leader)) {
+      // ---------------------------------------------------------- MMA issuer(s) (rank 0 of a pair)
       constexpr uint32_t idesc = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
       // descriptors of stage 0; stage s and K step k add (offset in bytes) / 16 to the
       // 14-bit start-address field (shared addresses stay below 2^18, so it cannot carry)
       const uint64_t adesc0 = smem_desc_k_sw128(base + C::kOffA);
       const uint64_t bdesc0 = smem_desc_k_sw128(base + C::kOffB);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
-        Tile ti;
-        if (!fetch_tile(t, ti)) continue;
-        for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
-          const uint32_t b = it % NB, tph = (it / NB) & 1u;
-          if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
-          if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t ad = adesc0 + ((s * C::kABytes) >> 4);
-          const uint64_t bd = bdesc0 + ((s * C::kBBytes) >> 4);
-          const uint32_t d_tmem = tmem_base + b * BN;
-          if constexpr (PAIR) {
+      if constexpr (!kLone) {
+        uint32_t it = 0;
+        bool ok = true;
+        for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
+          Tile ti;
+          if (!fetch_tile(t, ti)) continue;
+          for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
+            const uint32_t s = it % S, ph = (it / S) & 1u;
+            const uint32_t b = it % NB, tph = (it / NB) & 1u;
+            if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ad = adesc0 + ((s * C::kStageABytes) >> 4);
+            const uint64_t bd = bdesc0 + ((s * C::kStageBBytes) >> 4);
+            const uint32_t d_tmem = tmem_base + b * BN;
+            if constexpr (PAIR) {
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              mma_f8f6f4_pair_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-            mma_commit_pair_if(leader, empty(s), 0x3);  // both CTAs' stage s is free
-            mma_commit_pair_if(leader, tfull(b), 0x3);  // both CTAs' partial is ready
-          } else {
+              for (int k = 0; k < BK / 32; ++k)
+                mma_f8f6f4_pair(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+              mma_commit_pair(leader, empty(s), 0x3);  // both CTAs' stage s is free
+              mma_commit_pair(leader, tfull(b), 0x3);  // both CTAs' partial is ready
+            } else {
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              mma_f8f6f4_if(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-            // one commit per K block: the epilogue, on seeing the partial, also frees the stage
-            mma_commit_if(leader, tfull(b));
+              for (int k = 0; k < BK / 32; ++k)
+                mma_f8f6f4(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+              // one commit per K block: the epilogue, on seeing the partial, also frees the stage
+              mma_commit(leader, tfull(b));
+            }
+          }
+        }
+        if (!ok && it > 0 && leader) {  // wait for the MMAs already issued before TMEM is released
+          const uint32_t last = it - 1;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(tfull(last % NB), (last / NB) & 1u) && clock64() - t0 < a.budget) {
+          }
+        }
+      } else {
+        // Lone issuers: issuer mi takes the stages it % MW == mi.  Stage `it` (counted over this
+        // CTA's tiles) holds the K blocks kb0 .. kb0 + nk - 1 of its tile, nk = min(KPS, K blocks
+        // left); `kit` counts the K blocks of all earlier stages (the TMEM buffer sequence, as
+        // the epilogue counts them).
+        static_assert(MW == 2, "two lone issuers");
+        const uint32_t mi = static_cast<uint32_t>(warp - 1);
+        uint32_t it = 0, kit = 0;
+        bool ok = true, issued = false;
+        uint32_t last_bar = 0, last_ph = 0;  // latest commit to a TMEM-full barrier
+        bool full_seen = false, tmem_seen = false;  // early tests for the next own K block
+        for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
+          Tile ti;
+          if (!fetch_tile(t, ti)) continue;
+          for (int32_t kb0 = 0; kb0 < a.KB && ok; kb0 += KPS, ++it) {
+            const int32_t left = a.KB - kb0;
+            const uint32_t nk = static_cast<uint32_t>(left < KPS ? left : KPS);
+            if (it % MW == mi) {
+              const uint32_t s = it % S, ph = (it / S) & 1u;
+              if (!wait_seen(full_seen, full(s), ph, a, abort_flag)) { ok = false; break; }
+              full_seen = false;
+              for (uint32_t j = 0; j < nk; ++j) {
+                const uint32_t kj = kit + j;
+                const uint32_t b = kj % NB, tph = (kj / NB) & 1u;
+                if (!wait_seen(tmem_seen, tempty(b), tph ^ 1u, a, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // test the next own K block's barriers now; the MMAs below hide the round trip
+                uint32_t kn = kj + 1;
+                if (j + 1 == nk) {  // the next own K block opens stage it + MW, past the other
+                                    // issuer's stage (which may start the next tile)
+                  const int32_t p = kb0 + KPS < a.KB ? kb0 + KPS : 0;
+                  kn += static_cast<uint32_t>(a.KB - p < KPS ? a.KB - p : KPS);
+                  full_seen = mbar_test_wait(full((it + MW) % S), ((it + MW) / S) & 1u);
+                }
+                tmem_seen = mbar_test_wait(tempty(kn % NB), ((kn / NB) & 1u) ^ 1u);
+                const uint64_t ad = adesc0 + ((s * C::kStageABytes + j * C::kABytes) >> 4);
+                const uint64_t bd = bdesc0 + ((s * C::kStageBBytes + j * C::kBBytes) >> 4);
+                const uint32_t d_tmem = tmem_base + b * BN;
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k)
+                  mma_f8f6f4(true, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                mma_commit(true, tfull(b));
+                issued = true;
+                last_bar = tfull(b);
+                last_ph = tph;
+              }
+              if (!ok) break;
+              mma_commit(true, empty(s));  // the stage is free once these MMAs have read it
+            }
+            kit += nk;
+          }
+        }
+        if (!ok && issued) {  // wait for the MMAs already issued before TMEM is released
+          const long long t0 = clock64();
+          while (!mbar_try_wait(last_bar, last_ph) && clock64() - t0 < a.budget) {
           }
         }
       }
-      if (!ok && it > 0 && leader) {  // wait for the MMAs already issued before TMEM is released
-        const uint32_t last = it - 1;
-        const long long t0 = clock64();
-        while (!mbar_try_wait(tfull(last % NB), (last / NB) & 1u) && clock64() - t0 < a.budget) {
-        }
-      }
     }
+    __syncwarp();  // the other lanes of the producer and MMA warps wait for lane 0 here
   } else {
     if constexpr (C::kRebalance) regs_acquire<C::kRegsHigh>();
     // ------------------------------------------------------------ promotion + epilogue
@@ -453,8 +557,10 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     const int kpart = grp / C::kColGroups;                 // promotes K blocks kb % kKSplit == kpart
     const int col0 = (grp % C::kColGroups) * C::kEpiCols;  // column offset inside the tile
     const int row = q * 32 + lane;       // tile row owned by this thread
-    // one lane per K part frees the operand stage of each K block once its MMAs are done
-    const bool stage_releaser = !PAIR && lane == 0 && ew == kpart * 4 * C::kColGroups;
+    // one issuer: one lane per K part frees the operand stage of each K block once its MMAs
+    // are done (the tile's K blocks map one to one onto stages)
+    const bool stage_releaser =
+        C::kMmaWarps == 1 && !PAIR && lane == 0 && ew == kpart * 4 * C::kColGroups;
     // this warp's TMEM buffers are released on rank 0's barrier (its own CTA unless paired)
     auto release_tmem = [&](uint32_t b) {
       if (lane == 0) {
@@ -513,7 +619,6 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         const float scale = sa_kb * sb_kb;
         const float2 scale2 = make_float2(scale, scale);
         if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
-        // the MMAs of this K block are complete: its operand stage can be refilled
         if (stage_releaser) mbar_arrive(empty(it % S));
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
@@ -634,6 +739,7 @@ static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem")
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<128, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 
 template <int BN, int MODE, bool PAIR = false>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
@@ -691,12 +797,12 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
 
 thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0;
 
-// FP8G_PAIR=1 runs 256-wide tiles on CTA pairs.  Off by default: with two TMEM partial
-// buffers per CTA, the pair's cross-CTA hops lengthen the MMA / promotion hand-off more than the
-// deeper ring gains (measured ~10% slower on 4096 x 8192 x 8192).
-bool env_pair() {
+// FP8G_PAIR=1 runs 256-wide tiles as 256 x 256 CTA-pair tiles, FP8G_PAIR=2 as 256 x 128 pair
+// tiles (four TMEM partial buffers per CTA).  Off by default: measured no faster than single-CTA
+// 256-wide tiles (=1: within a few percent either way; =2: ~1.5x slower on 4096 x 8192 x 8192).
+int env_pair() {
   const char* e = std::getenv("FP8G_PAIR");
-  return e && e[0] == '1';
+  return (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) ? e[0] - '0' : 0;
 }
 
 // FP8G_BLOCK_N (64, 128 or 256) forces the tile width; read on every call.
@@ -746,12 +852,15 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
   if (o.rows == 0) return FP8G_OK;
 
   const int64_t m_blocks = (MODE == kMasked) ? o.E * ((o.cap + BM - 1) / BM) : (o.rows + BM - 1) / BM;
-  const int bn = choose_block_n(m_blocks, o.N, dev->sm_count);
+  int bn = choose_block_n(m_blocks, o.N, dev->sm_count);
   // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
   const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
-  // 256-wide tiles run as CTA pairs (256 x 256 per pair) unless there are too few rows
-  const bool pair = bn == 256 && env_pair() &&
+  // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
+  // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2)
+  const int pmode = env_pair();
+  const bool pair = bn == 256 && pmode != 0 &&
                     (MODE != kDense || (o.rows + BM - 1) / BM >= 2) && dev->sm_count >= 2;
+  if (pair && pmode == 2) bn = 128;
 
   GemmArgs a{};
   a.rows = static_cast<int32_t>(o.rows);
@@ -772,21 +881,25 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
   a.status = dev->status;
   a.budget = wait_budget_cycles();
 
+  // K blocks per stage of the variant launched below (its Cfg::kKPS)
+  const uint32_t kps = small_m ? Cfg<64, true>::kKPS : 1u;
   CUtensorMap tA, tB, tD;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(o.K), static_cast<uint64_t>(o.rows)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(o.lda)};
-    const uint32_t box[2] = {BK, small_m ? 64u : static_cast<uint32_t>(BM)};
-    if ((st = encode_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, o.A, dims, strides, box,
+    // A as [K/128][rows][128]: a box is kps K blocks of the tile's rows
+    const uint64_t dims[3] = {BK, static_cast<uint64_t>(o.rows), static_cast<uint64_t>(o.K / BK)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(o.lda), BK};
+    const uint32_t box[3] = {BK, small_m ? 64u : static_cast<uint32_t>(BM), kps};
+    if ((st = encode_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, o.A, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
       return st;
   }
   {
-    const uint64_t dims[3] = {static_cast<uint64_t>(o.K), static_cast<uint64_t>(o.N),
+    // B as [E][K/128][N][128]
+    const uint64_t dims[4] = {BK, static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.K / BK),
                               static_cast<uint64_t>(o.E)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(o.ldb), static_cast<uint64_t>(o.ldb * o.N)};
-    const uint32_t box[3] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn), 1};
-    if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, o.B, dims, strides, box,
+    const uint64_t strides[3] = {static_cast<uint64_t>(o.ldb), BK, static_cast<uint64_t>(o.ldb * o.N)};
+    const uint32_t box[4] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn), kps, 1};
+    if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, o.B, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
       return st;
   }
@@ -822,6 +935,11 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
       t_last_stages = Cfg<256>::kStages;
       return launch_kernel<256, MODE>(a, tA, tB, tD, grid, table_entries, stream);
     case 128:
+      if (pair) {
+        t_last_stages = Cfg<128, false, true>::kStages;
+        return launch_kernel<128, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
+                                                                               table_entries, stream);
+      }
       t_last_stages = Cfg<128>::kStages;
       return launch_kernel<128, MODE>(a, tA, tB, tD, grid, table_entries, stream);
     default:

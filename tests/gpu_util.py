@@ -95,9 +95,10 @@ def block_n(bn):
     return env_var("FP8G_BLOCK_N", bn or None)
 
 
-def pair(on):
-    """Turn the CTA-pair kernel for 256-wide tiles on or off (FP8G_PAIR)."""
-    return env_var("FP8G_PAIR", 1 if on else None)
+def pair(mode):
+    """CTA pairs inside the block (FP8G_PAIR): 0 / False off, 1 / True 256 x 256 pair tiles,
+    2 for 256 x 128 pair tiles."""
+    return env_var("FP8G_PAIR", int(mode) if mode else None)
 
 
 def check_status():

@@ -56,6 +56,7 @@ def _dense_gpu(qa, sa, qb, sb, bn=None):
     (128, 256, 512, None), (1, 16, 128, 64), (64, 64, 128, None), (200, 208, 384, 256),
     (200, 208, 384, 128), (200, 208, 384, 64), (300, 512, 1024, 256), (129, 272, 256, 128),
     (64, 1792, 7168, 64), (257, 1024, 640, 256), (513, 384, 256, None),
+    (40, 256, 384, 64), (17, 128, 1152, 64),  # small M, odd K-block counts (part-filled stages)
 ])
 def test_dense_small_shapes(M, N, K, bn):
     qa, sa, qb, sb = _problem(M, N, K, seed=M * 7 + N + K)
@@ -63,14 +64,16 @@ def test_dense_small_shapes(M, N, K, bn):
     assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} bn={bn}")
 
 
-@pytest.mark.parametrize("use_pair", [True, False])
+@pytest.mark.parametrize("use_pair", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 128), (300, 272, 384), (640, 768, 1024), (129, 512, 256)])
 def test_dense_256_wide_single_cta_and_pair(M, N, K, use_pair):
     qa, sa, qb, sb = _problem(M, N, K, seed=M + 3 * N + K)
     with pair(use_pair):
         D = _dense_gpu(qa, sa, qb, sb, 256)
         cfg = g.fp8g_last_config()
-    assert cfg["block_n"] == 256 and (cfg["stages"] == 6) == (use_pair and M > 128)
+    paired = use_pair and M > 128  # a single m-block never runs as a pair
+    want = {0: (256, 4), 1: (256, 6), 2: (128, 8)}[use_pair if paired else 0]
+    assert (cfg["block_n"], cfg["stages"]) == want
     assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} pair={use_pair}")
 
 
@@ -180,7 +183,7 @@ def _contig_gpu(qa, sa, qb, sb, offs, bn=None):
     return D
 
 
-@pytest.mark.parametrize("bn,use_pair", [(None, True), (256, True), (256, False), (128, True), (64, True)])
+@pytest.mark.parametrize("bn,use_pair", [(None, 1), (256, 1), (256, 0), (128, 1), (64, 1), (None, 2), (256, 2)])
 def test_contiguous_small(bn, use_pair):
     qa, sa, qb, sb, offs = _contig_problem([100, 0, 300, 128, 1], N=272, K=384, seed=5, extra_rows=128)
     with pair(use_pair):
@@ -255,7 +258,7 @@ def _masked_problem(E, cap, N, K, seed):
     return qa.reshape(E, cap, K), sa.reshape(E, cap, -1), np.stack(qbs), np.stack(sbs)
 
 
-@pytest.mark.parametrize("bn,use_pair", [(None, True), (256, True), (256, False), (128, True), (64, True)])
+@pytest.mark.parametrize("bn,use_pair", [(None, 1), (256, 1), (256, 0), (128, 1), (64, 1), (None, 2), (256, 2)])
 def test_masked_small(bn, use_pair):
     E, cap, N, K = 5, 160, 272, 384
     masked = [0, 1, 160, 37, 129]
