@@ -24,6 +24,7 @@ Multi-GPU: one process per GPU under torchrun; every rank runs an independent re
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -268,10 +269,10 @@ def run_ours(args, world, rank, local, dist):
     if g.fp8g_get_status() != 0:
         raise RuntimeError("device status not OK after setup")
 
-    def one_step(record):
+    def one_step(record, evs):
         for i, c in enumerate(cases):
             flush.fill_(i & 0xFF)
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev = evs[i]
             ev[0].record(stream)
             c.quantize()
             ev[1].record(stream)
@@ -281,20 +282,32 @@ def run_ours(args, world, rank, local, dist):
 
     launches_per_step = 2 * len(cases)
     records = []
-    with ClockSampler(local) as clk:  # started before the warm-up: nvidia-smi needs a moment
-        for _ in range(args.warmup):
-            one_step([])
-        torch.cuda.synchronize()
-        barrier(dist)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        w0 = time.time()
-        for _ in range(args.steps):
-            one_step(records)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        clk.mark(w0, time.time())
-        barrier(dist)
+    # Events are made before the timed region and the garbage collector is paused during it: a
+    # host pause long enough to drain the queued work would otherwise leave the GPU idle between
+    # two events of a short kernel and count that idle time.
+    spare = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in cases]
+    timed_evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in cases]
+                 for _ in range(args.steps)]
+    gc_was_on = gc.isenabled()
+    gc.disable()
+    try:
+        with ClockSampler(local) as clk:  # started before the warm-up: nvidia-smi needs a moment
+            for _ in range(args.warmup):
+                one_step([], spare)
+            torch.cuda.synchronize()
+            barrier(dist)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            w0 = time.time()
+            for k in range(args.steps):
+                one_step(records, timed_evs[k])
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+            clk.mark(w0, time.time())
+            barrier(dist)
+    finally:
+        if gc_was_on:
+            gc.enable()
     st = g.fp8g_get_status()
     if st != 0:
         raise RuntimeError(f"device status {g.STATUS.get(st, st)} after the timed region")

@@ -58,8 +58,26 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, flo
   return w;
 }
 
+// Direct path.  For most blocks the single product y = RN(x * RN(1/s)) already has the code of
+// RN(x / s) for every bf16 x with |x| <= amax, and no bracket is needed.  Whether it does depends
+// only on amax's 8-bit bf16 significand A (with s normal, s, 1/s, the products and the codes all
+// scale exactly with a power-of-two change of amax and x), so an exhaustive enumeration over A and
+// every x settles it: bit (A - 128) of the kDirectSafe words is set when no x gives a different code (102 of
+// the 128 significands).  gen_quant_tables.py, next to this package, produces the table.
+constexpr uint32_t kDirectSafe0 = 0xFCFFFBEFu, kDirectSafe1 = 0x7EB9BB37u,  // A = 128..159, 160..191
+                   kDirectSafe2 = 0xFFDACFA7u, kDirectSafe3 = 0xF2FFF7FFu;  // A = 192..223, 224..255
+
+// True when the block's codes can be taken from the direct product (amax as a float holding a
+// bf16 value; s its scale).
+__device__ __forceinline__ bool direct_ok(float amax, float s) {
+  const uint32_t a7 = (__float_as_uint(amax) >> 16) & 0x7Fu;  // amax's stored mantissa bits
+  const uint32_t word = a7 < 64u ? (a7 < 32u ? kDirectSafe0 : kDirectSafe1)
+                                 : (a7 < 96u ? kDirectSafe2 : kDirectSafe3);
+  return s >= 1.17549435e-38f && ((word >> (a7 & 31u)) & 1u) != 0u;
+}
+
 template <int N>
-__device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (&w)[N / 4]) {
+__device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direct, uint32_t (&w)[N / 4]) {
   static_assert(N % 4 == 0, "N");
   if (s == 0.0f) {
 #pragma unroll
@@ -67,6 +85,17 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (
     return;
   }
   bool exact = !(s >= 1.17549435e-38f);  // subnormal s: divide every element
+  if (!exact && direct) {
+    const float r = __frcp_rn(s);
+    const float2 r2 = make_float2(r, r);
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float2 y01 = __fmul2_rn(make_float2(f[4 * i], f[4 * i + 1]), r2);
+      const float2 y23 = __fmul2_rn(make_float2(f[4 * i + 2], f[4 * i + 3]), r2);
+      w[i] = cvt_e4m3x4(y01.x, y01.y, y23.x, y23.y);
+    }
+    return;
+  }
   if (!exact) {
     const float r = __frcp_rn(s);
     const float lo_f = __fmul_rn(r, 1.0f - 0x1p-20f), hi_f = __fmul_rn(r, 1.0f + 0x1p-20f);
@@ -90,9 +119,9 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t (
   }
 }
 
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, bool direct) {
   uint32_t w[2];
-  quant_n<8>(f, s, w);
+  quant_n<8>(f, s, direct, w);
   return make_uint2(w[0], w[1]);
 }
 
@@ -141,7 +170,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
       const float s = __fdiv_rn(a, kE4M3Max);
       if (base + u * n_groups < total) {
         uint32_t c[4];
-        quant_n<16>(f, s, c);
+        quant_n<16>(f, s, direct_ok(a, s), c);
         uint8_t* dst = q + m[u] * ldq + kb[u] * 128 + sub * 8;
         *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
         *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
@@ -183,13 +212,14 @@ __global__ void __launch_bounds__(256) quantize_128x128_kernel(
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   const float s = __fdiv_rn(amax, kE4M3Max);
+  const bool direct = direct_ok(amax, s);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = r0 + 16 * i;
     if (r < rows) {
       float f[8];
       unpack8(raw[i], f);
-      *reinterpret_cast<uint2*>(qb + static_cast<int64_t>(r) * K) = quant8(f, s);
+      *reinterpret_cast<uint2*>(qb + static_cast<int64_t>(r) * K) = quant8(f, s, direct);
     }
   }
   if (t == 0) sB[(e * NB + nb) * KB + kb] = s;

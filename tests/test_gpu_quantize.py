@@ -146,3 +146,27 @@ def test_1x128_quotients_on_every_rounding_midpoint():
             rows.append(blk * sign * 2.0 ** k)
     x = torch.stack(rows).to(torch.bfloat16)
     _check_1x128(x)
+
+
+def test_1x128_every_amax_significand_against_every_x():
+    # One block per (amax significand A, chunk of x): element 0 is amax, the rest are bf16 values
+    # +-X * 2^-k with |x| <= amax, so every (A, x) pair the code decision depends on is covered,
+    # for marked significands (direct product) and unmarked ones (bracket) alike, at three amax
+    # exponents.
+    X = np.arange(128, 256, dtype=np.float64) / 128.0
+    rows = []
+    for scale in (1.0, 2.0 ** -30, 2.0 ** 40):
+        for A in range(128, 256):
+            amax = A / 128.0
+            x = np.concatenate([X * 2.0 ** -k for k in range(32)])
+            x = x[x <= amax]
+            x = np.concatenate([x, -x])
+            for i in range(0, x.size, 127):
+                row = np.zeros(128)
+                row[0] = amax
+                chunk = x[i:i + 127]
+                row[1:1 + chunk.size] = chunk
+                rows.append(row * scale)
+    xt = torch.from_numpy(np.stack(rows)).to(torch.bfloat16)
+    assert torch.equal(xt.double(), torch.from_numpy(np.stack(rows)))  # every value is a bf16
+    _check_1x128(xt)
