@@ -230,22 +230,29 @@ class Case:
             g.fp8_grouped_gemm_masked(self.qA.view(w.E, w.cap, w.K), self.sA, self.qB, self.sB, D, self.meta)
 
 
-def source_digest() -> str:
+# the sources each kernel is built from (a kernel's counters go stale when one of these changes)
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "common.cuh"), "quant": ("quantize.cu", "ptx.cuh", "common.cuh")}
+
+
+def source_digest(kind: str | None = None) -> str:
+    """Digest of csrc/ (kind None) or of the files one kernel kind is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_grouped_gemm_block_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = sorted(os.listdir(csrc)) if kind is None else sorted(KERNEL_SOURCES[kind])
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel's source."""
+    digest = source_digest(kernel_key.split(":")[0])
     try:
         with open(TRAFFIC_PATH) as f:
             for line in f:
                 parts = line.split("#")[0].split()
-                if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == source_digest():
+                if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == digest:
                     return float(parts[2])
     except OSError:
         pass
