@@ -32,6 +32,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -98,7 +101,7 @@ struct Cfg {
   static constexpr uint32_t kOffOut = kOffB + kStages * kStageBBytes;
   static constexpr uint32_t kOffX = kOffOut + kStoreWarps * kOutBytes;
   static constexpr uint32_t kOffBar = kOffX + kXBytes;
-  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kTmemBufs + 2;
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kTmemBufs + 4;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
@@ -122,6 +125,13 @@ struct GemmArgs {
   const int32_t* groups;  // contiguous: offsets [E+1]; masked: counts [E]
   unsigned int* status;
   long long budget;
+  // stream-K tail (see make_work): on/off, its minimum K blocks per CTA, and the workspace of
+  // FP32 partial tiles (one slot per CTA) with one ready flag per CTA (zeroed before the launch)
+  int32_t sk;
+  int32_t sk_min_units;
+  int32_t sk_min_gain;  // split only when it saves at least this many K blocks per CTA
+  float4* ws_part;
+  uint32_t* ws_flag;
 };
 
 struct Tile {
@@ -130,6 +140,93 @@ struct Tile {
   int32_t g;      // expert
   int32_t rows;   // rows of the tile that may be stored (masked tail), else BM
 };
+
+// The work of one CTA, as pieces (tile, K blocks kb0 .. kb1 - 1).  Whole tiles c, c + G, ...
+// come first.  With the stream-K tail on, only the whole rounds of tiles are dealt that way; the
+// K blocks of the R < G tiles left over are then split evenly over the G CTAs (CTA c takes units
+// [c*u, (c+1)*u) of the tail's R*KB, u >= sk_min_units), so the last round no longer leaves most
+// SMs idle.  A tile split between CTAs is finished by the CTA holding its first K blocks (it
+// reaches them at the end of its share, when the others have written their partial sums): it
+// adds the partials of CTAs c_lo .. c_hi and stores.  The others (kContrib) write their FP32
+// partial to their workspace slot and raise their flag.  Each CTA has at most one piece of each
+// of the two kinds.
+enum PieceKind : int32_t { kWhole = 0, kFinish = 1, kContrib = 2 };
+struct Piece {
+  int32_t t, kb0, kb1, kind, c_lo, c_hi;
+};
+struct Work {
+  int32_t G, KB, c;
+  int32_t t, t_end;           // whole tiles t, t + G, ... below t_end
+  int32_t tail0, u;           // first tail tile, tail K blocks per CTA
+  int32_t unit, unit_end;     // this CTA's tail units
+};
+__device__ __forceinline__ Work make_work(int32_t num_tiles, int32_t G, int32_t c, int32_t KB, bool sk,
+                                          int32_t min_units, int32_t min_gain) {
+  Work w;
+  w.G = G;
+  w.KB = KB;
+  w.c = c;
+  w.t = c;
+  if (!sk) {
+    w.t_end = num_tiles;
+    w.tail0 = num_tiles;
+    w.u = 1;
+    w.unit = w.unit_end = 0;
+    return w;
+  }
+  w.tail0 = (num_tiles / G) * G;
+  w.t_end = w.tail0;
+  const int64_t U = static_cast<int64_t>(num_tiles - w.tail0) * KB;
+  int64_t u = (U + G - 1) / G;
+  const int64_t umin = min_units < KB ? min_units : KB;
+  if (u < umin) u = umin;
+  if (KB - u < min_gain) {  // the split would not pay for its partial-sum traffic: whole tiles
+    w.t_end = num_tiles;
+    w.tail0 = num_tiles;
+    w.u = 1;
+    w.unit = w.unit_end = 0;
+    return w;
+  }
+  w.u = static_cast<int32_t>(u);
+  const int64_t s0 = static_cast<int64_t>(c) * u;
+  w.unit = static_cast<int32_t>(s0 < U ? s0 : U);
+  w.unit_end = static_cast<int32_t>(s0 + u < U ? s0 + u : U);
+  return w;
+}
+__device__ __forceinline__ bool next_piece(Work& w, Piece& p) {
+  if (w.t < w.t_end) {
+    p.t = w.t;
+    p.kb0 = 0;
+    p.kb1 = w.KB;
+    p.kind = kWhole;
+    p.c_lo = 0;
+    p.c_hi = -1;
+    w.t += w.G;
+    return true;
+  }
+  if (w.unit < w.unit_end) {
+    const int32_t r = w.unit / w.KB, kb0 = w.unit - r * w.KB;
+    const int32_t take = min(w.KB - kb0, w.unit_end - w.unit);
+    p.t = w.tail0 + r;
+    p.kb0 = kb0;
+    p.kb1 = kb0 + take;
+    if (kb0 == 0 && p.kb1 == w.KB) {
+      p.kind = kWhole;
+      p.c_lo = 0;
+      p.c_hi = -1;
+    } else if (kb0 == 0) {  // the other units of tile r belong to the following CTAs
+      p.kind = kFinish;
+      p.c_lo = (r * w.KB + p.kb1) / w.u;
+      p.c_hi = (r * w.KB + w.KB - 1) / w.u;
+    } else {
+      p.kind = kContrib;
+      p.c_lo = p.c_hi = w.c;
+    }
+    w.unit += take;
+    return true;
+  }
+  return false;
+}
 
 // Tile index -> tile.  Returns false when the tile has no rows to compute.
 template <int BN, int MODE>
@@ -250,6 +347,23 @@ __device__ __forceinline__ bool wait_seen(bool seen, uint32_t bar, uint32_t pari
   return seen || wait_bounded(bar, parity, a, abort_flag);
 }
 
+// Bounded wait for another CTA's flag (stream-K partial written).  On timeout: flag this CTA,
+// record the status.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, const GemmArgs& a, volatile int* abort_flag) {
+  if (ld_acquire_gpu(f) != 0u) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(f) == 0u) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > a.budget) {
+      *abort_flag = 1;
+      record_status(a.status, FP8G_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 template <int BN, int MODE, bool PAIR = false>
 __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -274,6 +388,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + NB + b); };
   const uint32_t xfull = bar0 + 8u * (2 * S + 2 * NB);  // K-split exchange written
   const uint32_t xempty = xfull + 8u;                             // K-split exchange read
+  const uint32_t sk_written = xfull + 16u;  // stream-K: every epilogue warp has written its partial
+  const uint32_t sk_ready = xfull + 24u;    // stream-K: the partials to add are complete
   // misc: [0] TMEM base, [1] abort flag, [2] group table out of contract
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -292,6 +408,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     }
     mbar_init(xfull, C::kStoreWarps);
     mbar_init(xempty, C::kStoreWarps);
+    mbar_init(sk_written, C::kEpiWarps);
+    mbar_init(sk_ready, 1);
     misc[1] = 0;
     misc[2] = 0;  // set when the group table is out of contract
     fence_mbar_init();
@@ -388,6 +506,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     }
   };
   if (MODE == kContiguous && misc[2]) num_tiles = 0;
+  // stream-K tail: single-CTA tiles with one K part and one issuer only
+  const bool sk_on = !PAIR && C::kKSplit == 1 && C::kMmaWarps == 1 && a.sk != 0;
   if (warp < C::kEpiWarp0) {
     if constexpr (C::kRebalance) regs_release<C::kRegsLow>();
     const bool leader = lane == 0;
@@ -408,11 +528,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       uint32_t it = 0;  // stages filled
       bool ok = true;
       bool empty_seen = false;  // early test of the next stage's empty barrier (lone form)
-      for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
+      Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+      Piece pc;
+      while (ok && next_piece(w, pc)) {
         Tile ti;
-        if (!fetch_tile(t, ti)) continue;
+        if (!fetch_tile(pc.t, ti)) continue;
         // the K blocks of a stage past the end of K are zero-filled and never read
-        for (int32_t kb = 0; kb < a.KB; kb += KPS, ++it) {
+        for (int32_t kb = pc.kb0; kb < pc.kb1; kb += KPS, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           bool ready;
           if constexpr (kLone) {
@@ -455,10 +577,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       if constexpr (!kLone) {
         uint32_t it = 0;
         bool ok = true;
-        for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
+        Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+        Piece pc;
+        while (ok && next_piece(w, pc)) {
           Tile ti;
-          if (!fetch_tile(t, ti)) continue;
-          for (int32_t kb = 0; kb < a.KB; ++kb, ++it) {
+          if (!fetch_tile(pc.t, ti)) continue;
+          for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
             const uint32_t s = it % S, ph = (it / S) & 1u;
             const uint32_t b = it % NB, tph = (it / NB) & 1u;
             if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
@@ -499,9 +623,11 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         bool ok = true, issued = false;
         uint32_t last_bar = 0, last_ph = 0;  // latest commit to a TMEM-full barrier
         bool full_seen = false, tmem_seen = false;  // early tests for the next own K block
-        for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
+        Work w = make_work(num_tiles, tile_step, tile0, a.KB, false, 0, 0);  // whole tiles
+        Piece pc;
+        while (ok && next_piece(w, pc)) {
           Tile ti;
-          if (!fetch_tile(t, ti)) continue;
+          if (!fetch_tile(pc.t, ti)) continue;
           for (int32_t kb0 = 0; kb0 < a.KB && ok; kb0 += KPS, ++it) {
             const int32_t left = a.KB - kb0;
             const uint32_t nk = static_cast<uint32_t>(left < KPS ? left : KPS);
@@ -572,9 +698,15 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
     uint32_t it_base = 0, tiles_done = 0;
     bool ok = true;
-    for (int32_t t = tile0; t < num_tiles && ok; t += tile_step) {
+    // stream-K workspace slot of this thread: float4 j of thread e sits at slot[j * kEpiThreads + e]
+    constexpr int kEpiThreads = C::kEpiWarps * 32;
+    constexpr int64_t kSlotF4 = static_cast<int64_t>(kEpiThreads) * (C::kEpiCols / 4);
+    const int e_thr = ew * 32 + lane;
+    Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+    Piece pc;
+    while (ok && next_piece(w, pc)) {
       Tile ti;
-      if (!fetch_tile(t, ti)) continue;
+      if (!fetch_tile(pc.t, ti)) continue;
       const int32_t ncol0 = ti.n0 + col0;
       const bool has_cols = ncol0 < a.N;
       // small-M tiles: warps whose rows are all past M skip the promotion (nothing to store)
@@ -582,9 +714,9 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
       // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
       // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
-      int32_t sb_base = 0;
-      float sb_cur = (has_cols && lane < a.KB) ? ld_nc_f32(sbp + lane) : 0.0f;
-      float sb_nxt = (has_cols && lane + 32 < a.KB) ? ld_nc_f32(sbp + 32 + lane) : 0.0f;
+      int32_t sb_base = pc.kb0 & ~31;
+      float sb_cur = (has_cols && sb_base + lane < a.KB) ? ld_nc_f32(sbp + sb_base + lane) : 0.0f;
+      float sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
       // A-row scale of this thread's row, read from global memory kSAAhead K-block steps
       // before use (coalesced: a warp reads 32 consecutive rows of one K block)
       const int32_t grow = ti.a_row + row;
@@ -593,14 +725,14 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       float sa_q[kSAAhead];
 #pragma unroll
       for (int i = 0; i < kSAAhead; ++i) {
-        const int32_t kbi = kpart + i * C::kKSplit;
-        sa_q[i] = (row_ok && kbi < a.KB) ? ld_nc_f32(sap + static_cast<int64_t>(kbi) * a.ld_sa) : 0.0f;
+        const int32_t kbi = pc.kb0 + kpart + i * C::kKSplit;
+        sa_q[i] = (row_ok && kbi < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbi) * a.ld_sa) : 0.0f;
       }
       float2 acc[C::kEpiCols / 2];
 #pragma unroll
       for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-      for (int32_t kb = kpart; kb < a.KB; kb += C::kKSplit) {
-        const uint32_t it = it_base + kb;
+      for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += C::kKSplit) {
+        const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
         const uint32_t b = it % NB, tph = (it / NB) & 1u;
         const float sa_kb = sa_q[0];
 #pragma unroll
@@ -608,7 +740,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         {
           const int32_t kbn = kb + kSAAhead * C::kKSplit;
           sa_q[kSAAhead - 1] =
-              (row_ok && kbn < a.KB) ? ld_nc_f32(sap + static_cast<int64_t>(kbn) * a.ld_sa) : 0.0f;
+              (row_ok && kbn < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbn) * a.ld_sa) : 0.0f;
         }
         if (kb >= sb_base + 32) {
           sb_base += 32;
@@ -642,7 +774,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
           release_tmem(b);
         }
       }
-      it_base += a.KB;
+      it_base += static_cast<uint32_t>(pc.kb1 - pc.kb0);
       if (!ok) break;
       if constexpr (C::kKSplit > 1) {
         // add the odd-K-block partial sums (second warpgroup) into the first warpgroup's
@@ -669,6 +801,42 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(xempty);
+      }
+      if (pc.kind == kContrib) {
+        // part of a split tile: the FP32 partial goes to this CTA's workspace slot (L2), then
+        // the flag is raised once every epilogue warp has written its share
+        float4* slot = a.ws_part + static_cast<int64_t>(blockIdx.x) * kSlotF4;
+#pragma unroll
+        for (int j = 0; j < C::kEpiCols / 4; ++j)
+          __stcg(slot + static_cast<int64_t>(j) * kEpiThreads + e_thr,
+                 make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y));
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sk_written);
+        if (ew == 0 && lane == 0 && wait_bounded(sk_written, 0u, a, abort_flag))
+          st_release_gpu(a.ws_flag + blockIdx.x, 1u);
+        continue;
+      }
+      if (pc.kind == kFinish) {
+        // first K blocks of a split tile: add the partials of CTAs c_lo .. c_hi once their
+        // flags are up (one thread waits; it releases the others even on a timeout)
+        if (ew == 0 && lane == 0) {
+          bool got = true;
+          for (int32_t c2 = pc.c_lo; c2 <= pc.c_hi && got; ++c2) got = wait_flag(a.ws_flag + c2, a, abort_flag);
+          mbar_arrive(sk_ready);
+        }
+        if (!__all_sync(0xffffffffu, wait_bounded(sk_ready, 0u, a, abort_flag))) { ok = false; break; }
+        for (int32_t c2 = pc.c_lo; c2 <= pc.c_hi; ++c2) {
+          const float4* slot = a.ws_part + static_cast<int64_t>(c2) * kSlotF4;
+#pragma unroll
+          for (int j = 0; j < C::kEpiCols / 4; ++j) {
+            const float4 v = __ldcg(slot + static_cast<int64_t>(j) * kEpiThreads + e_thr);
+            acc[2 * j].x += v.x;
+            acc[2 * j].y += v.y;
+            acc[2 * j + 1].x += v.z;
+            acc[2 * j + 1].y += v.w;
+          }
+        }
       }
       // ---- epilogue: this warp holds rows q*32 .. q*32+31, columns ncol0 .. ncol0+kEpiCols-1
       const int nvalid = min(32, ti.rows - q * 32);
@@ -791,8 +959,73 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     }
     return FP8G_OK;
   }
+  if (args.sk) {
+    // stream-K: a CTA finishing a split tile waits for other CTAs' partials, so every CTA must
+    // be resident at once -- a cooperative launch guarantees it (one CTA per SM, grid <= SMs)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, args) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8G_ERR_CUDA;
+    }
+    return FP8G_OK;
+  }
   kern<<<grid, C::kThreads, smem, stream>>>(tA, tB, tD, args);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+// Stream-K workspace: one per (device, stream), allocated on the first call that needs it and
+// kept for the life of the process.  Per stream, because launches on different streams may run
+// at the same time; launches on one stream run in order and reuse it.  It holds one FP32
+// partial-tile slot per SM (128 x 128 columns x 2 column groups at most) and one flag per SM.
+constexpr size_t kSkSlotBytes = static_cast<size_t>(BM) * 256 * 4;
+struct SkWorkspace {
+  void* base = nullptr;
+  size_t flag_offset = 0;
+};
+std::mutex g_sk_mutex;
+std::map<std::pair<int, cudaStream_t>, SkWorkspace>* g_sk_ws = nullptr;
+
+// The workspace of (device, stream), or false when there is none and it cannot be made now
+// (allocation failed, or the stream is being captured into a graph: no allocation inside a
+// capture -- the call then runs without the stream-K tail).
+bool sk_workspace(int dev, int sm_count, cudaStream_t stream, float4** part, uint32_t** flags) {
+  std::lock_guard<std::mutex> lock(g_sk_mutex);
+  if (!g_sk_ws) g_sk_ws = new std::map<std::pair<int, cudaStream_t>, SkWorkspace>();
+  SkWorkspace& w = (*g_sk_ws)[{dev, stream}];
+  if (!w.base) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return false;
+    }
+    const size_t part_bytes = kSkSlotBytes * static_cast<size_t>(sm_count);
+    const size_t flag_bytes = (static_cast<size_t>(sm_count) * 4 + 255) / 256 * 256;
+    void* p = nullptr;
+    if (cudaMalloc(&p, part_bytes + flag_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    w.base = p;
+    w.flag_offset = part_bytes;
+  }
+  *part = static_cast<float4*>(w.base);
+  *flags = reinterpret_cast<uint32_t*>(static_cast<char*>(w.base) + w.flag_offset);
+  return true;
+}
+
+// FP8G_STREAMK=0 turns the stream-K tail off (read on every call).
+bool env_streamk() {
+  const char* e = std::getenv("FP8G_STREAMK");
+  return !(e && e[0] == '0' && e[1] == 0);
 }
 
 thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0;
@@ -914,6 +1147,35 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
 
   int64_t tiles_upper = (MODE == kMasked) ? m_blocks * a.num_n : static_cast<int64_t>(a.num_tiles);
   int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(tiles_upper, 1), dev->sm_count));
+  // stream-K tail for single-CTA tiles of width >= 128 (one K part, one MMA issuer) when the
+  // tiles do not fill whole rounds of the grid (masked: the count is only known on the device)
+  a.sk = 0;
+  a.sk_min_units = 8;
+  // a split tile costs its CTAs ~8-9 us (FP32 partial written, read back and added, and one more
+  // tile hand-off), about 20 K blocks of MMA time: split only when that gains clearly more
+  a.sk_min_gain = 24;
+  // (the same split rule as make_work on the device; the masked tile count is only known there)
+  auto tail_splits = [&](int64_t T) {
+    const int64_t G = dev->sm_count, KB = a.KB;
+    const int64_t U = (T - T / G * G) * KB;
+    int64_t u = (U + G - 1) / G;
+    const int64_t umin = a.sk_min_units < KB ? a.sk_min_units : KB;
+    if (u < umin) u = umin;
+    return U > 0 && KB - u >= a.sk_min_gain;
+  };
+  if (!pair && !small_m && bn >= 128 && env_streamk() &&
+      (MODE == kMasked || tail_splits(a.num_tiles))) {
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    if (sk_workspace(dev_id, dev->sm_count, stream, &a.ws_part, &a.ws_flag)) {
+      if (cudaMemsetAsync(a.ws_flag, 0, static_cast<size_t>(dev->sm_count) * 4, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8G_ERR_CUDA;
+      }
+      a.sk = 1;
+      grid = dev->sm_count;  // every SM takes a share of the tail
+    }
+  }
   int table_entries = (MODE == kDense) ? 0 : static_cast<int>(o.E + 1);
   if (pair) {
     // pair tiles: dense ceil(num_m/2) x num_n; grouped at most (m-blocks + experts)/2 x num_n

@@ -280,6 +280,16 @@ __device__ __forceinline__ void tma_load_4d_pair(bool pred, uint32_t dst, const 
       : "memory");
 }
 
+// ---------------------------------------------------------------- cross-CTA flags (global memory)
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;

@@ -15,7 +15,7 @@ import torch
 import moe_grouped_gemm_block_gb300 as g
 from moe_grouped_gemm_block_gb300.workloads import WORKLOADS, make_inputs, round_up
 from oracle import gemm_nt, grouped_contiguous, grouped_masked, quantize_128x128, quantize_1x128
-from tests.gpu_util import (assert_gemm_close, bf16_bits, bf16_to_np, block_n, check_status, need_gpu, pair,
+from tests.gpu_util import (assert_gemm_close, bf16_bits, bf16_to_np, block_n, check_status, env_var, need_gpu, pair,
                             sa_from_device, sa_to_device, u8)
 
 pytestmark = pytest.mark.gpu
@@ -332,3 +332,86 @@ def test_status_clear_after_many_calls_on_two_streams():
     check_status()
     for D in outs[1:]:
         assert torch.equal(D, outs[0])
+
+
+# ---------------------------------------------------------------- stream-K tail
+# With FP8G_STREAMK on (the default), tiles that do not fill whole rounds of the grid have their
+# K blocks split over all SMs when that saves at least 24 K blocks per CTA; CTAs holding part of a
+# tile write FP32 partials that the CTA with its first K blocks adds.  These shapes split tiles
+# (K = 4096: 32 K blocks, 8 per CTA), with and without a round of whole tiles before the tail.
+
+def streamk(on):
+    return env_var("FP8G_STREAMK", None if on else 0)
+
+
+@pytest.mark.parametrize("on", [True, False])
+@pytest.mark.parametrize("M,N,K,bn", [
+    (640, 768, 4096, 256),    # 15 tiles: every tile split among 4 CTAs
+    (300, 512, 4096, 128),    # 12 tiles of width 128, ragged M
+    (2560, 2048, 4096, 256),  # 160 tiles: one whole round, then 8 tiles split in four
+    (640, 768, 2048, 256),    # too few K blocks for a split to pay: whole tiles on every SM
+])
+def test_dense_stream_k_tail(M, N, K, bn, on):
+    qa, sa, qb, sb = _problem(M, N, K, seed=M + N + 7 * K)
+    with streamk(on):
+        D = _dense_gpu(qa, sa, qb, sb, bn)
+        cfg = g.fp8g_last_config()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-M // 128) * -(-N // bn)
+    kb = K // 128
+    u = max(-(-((tiles % sms) * kb) // sms), min(8, kb))
+    split = on and tiles % sms != 0 and kb - u >= 24  # the library's split rule
+    assert (cfg["grid"] == sms) == (split or tiles >= sms)
+    assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} bn={bn} streamk={on}")
+
+
+@pytest.mark.parametrize("on", [True, False])
+def test_contiguous_stream_k_tail(on):
+    qa, sa, qb, sb, offs = _contig_problem([300, 0, 128, 77], N=512, K=4096, seed=31, extra_rows=128)
+    with streamk(on):
+        D = _contig_gpu(qa, sa, qb, sb, offs, 256)
+    check_status()
+    init = np.full((qa.shape[0], qb.shape[1]), SENTINEL, np.uint16)
+    ref = grouped_contiguous(qa, sa, qb, sb, offs, init)
+    got = bf16_bits(D)
+    last = offs[-1]
+    assert np.array_equal(got[last:], ref[last:])  # rows outside every group: untouched
+    assert_gemm_close(bf16_to_np(D[:last]), ref[:last], f"contiguous streamk={on}")
+
+
+@pytest.mark.parametrize("on", [True, False])
+def test_masked_stream_k_tail(on):
+    E, cap, N, K = 4, 256, 512, 4096
+    masked = [256, 0, 130, 5]
+    qa, sa, qb, sb = _masked_problem(E, cap, N, K, seed=41)
+    with streamk(on):
+        D = _masked_gpu(qa, sa, qb, sb, masked, 256)
+    check_status()
+    ref = grouped_masked(qa, sa, qb, sb, masked, np.full((E, cap, N), SENTINEL, np.uint16))
+    got = bf16_bits(D)
+    for e in range(E):
+        m = masked[e]
+        assert np.all(got[e, m:] == SENTINEL), f"expert {e}: rows past masked_m written"
+        if m:
+            assert_gemm_close(bf16_to_np(D[e, :m]), ref[e, :m], f"masked e={e} streamk={on}")
+
+
+def test_stream_k_repeated_calls_and_two_streams():
+    # the per-stream workspace's flags are cleared before every launch: repeated calls, and calls
+    # alternating between two streams (each with its own workspace), give the same result
+    qa, sa, qb, sb = _problem(640, 768, 4096, seed=5)
+    ref = gemm_nt(qa, sa, qb, sb)
+    A, SA, B, SB = u8(qa), sa_to_device(sa), u8(qb), torch.from_numpy(sb).cuda()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    with block_n(256):
+        for i in range(6):
+            D = torch.empty((640, 768), dtype=torch.bfloat16, device="cuda")
+            with torch.cuda.stream(s1 if i % 2 else s2):
+                g.fp8_gemm_nt(A, SA, B, SB, D)
+            outs.append(D)
+    torch.cuda.synchronize()
+    check_status()
+    for D in outs:
+        assert torch.equal(D, outs[0])
+    assert_gemm_close(bf16_to_np(outs[0]), ref, "stream-K repeated")
