@@ -39,6 +39,14 @@
  *  - Only sm_103 devices are supported; anything else returns
  *    FP8G_ERR_UNSUPPORTED_DEVICE (there is no fallback path).
  *  - Calls are thread-safe; calls on different streams may run concurrently.
+ *  - GEMM workspace.  When a GEMM's tiles do not fill whole rounds of the grid, the
+ *    K blocks of the last, partial round may be split across all SMs (stream-K;
+ *    FP8G_STREAMK=0 turns this off).  The first such call on a stream allocates an
+ *    internal workspace for it -- 128 KiB per SM plus one flag per SM, about 19 MiB
+ *    on GB300 -- which the library keeps for the life of the process.  A call made
+ *    while its stream is being captured never allocates: if that stream has no
+ *    workspace yet, the call runs without the split.  fp8_gemm_nt_noalloc is the
+ *    variant that never allocates.
  */
 #ifndef FP8GEMM_H_
 #define FP8GEMM_H_
