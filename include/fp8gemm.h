@@ -115,6 +115,36 @@ int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa, cons
                 int64_t K, void* stream);
 
 /*
+ * fp8_gemm_nt_noalloc -- fp8_gemm_nt that never allocates device memory.  The
+ * pages have no counterpart of this call: it exists because of the library's own
+ * stream-K workspace (see "GEMM workspace" above).
+ *
+ * Some callers cannot let a library allocate while they run: an allocation can
+ * synchronise the device, or fail, in the middle of latency-critical work, and a
+ * framework that owns a fixed memory budget or serves allocations from its own
+ * pool expects every device buffer to come from it.  fp8_gemm_nt allocates its
+ * workspace on the first call on each stream that splits tiles; this call uses a
+ * fixed buffer that is part of the library's device image instead: 160 stream-K
+ * slots of 128 KiB plus 1 KiB of flags (20 MiB + 1 KiB, present once the library's
+ * kernels are loaded).  It does clear the flags with a memset on `stream` before
+ * each launch.
+ *
+ * Same arguments, results and errors as fp8_gemm_nt, plus:
+ *  - a device with more than 160 SMs is out of the buffer's range and gets
+ *    FP8G_ERR_INVALID_ARG (nothing launched);
+ *  - there is one buffer per device, shared by every call of this function on
+ *    that device: calls that overlap in time (on different streams, without an
+ *    ordering between them) race on it and corrupt each other's results, so the
+ *    caller must order them (one stream, or events);
+ *  - the first call on each device looks up the buffer's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call before
+ *    capturing any stream.
+ */
+int fp8_gemm_nt_noalloc(const void* A, int64_t lda, const float* sA, int64_t ld_sa, const void* B,
+                        int64_t ldb, const float* sB, void* D, int64_t ldd, int64_t M, int64_t N,
+                        int64_t K, void* stream);
+
+/*
  * fp8_grouped_gemm_contiguous -- MoE grouped GEMM, contiguous layout
  * ("DeepGEMM explainer" sec. 3.2 and 4.2; "DeepGEMM FP8 walk-through" sec. 5.3:
  * pass each group's id and token offset; keep each expert's rows contiguous and

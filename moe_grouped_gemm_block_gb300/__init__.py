@@ -48,6 +48,7 @@ _SIGNATURES = {
     "fp8_quantize_1x128": [_P, _I64, _I64, _I64, _P, _I64, _FP, _I64, _P],
     "fp8_quantize_128x128": [_P, _I64, _I64, _I64, _P, _FP, _P],
     "fp8_gemm_nt": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
+    "fp8_gemm_nt_noalloc": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_contiguous": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_masked": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8g_get_status": [_P],
@@ -139,6 +140,21 @@ def fp8_gemm_nt(A, sA, B, sB, D) -> None:
     ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
     _check(lib().fp8_gemm_nt(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
                              _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt")
+
+
+def fp8_gemm_nt_noalloc(A, sA, B, sB, D) -> None:
+    """fp8_gemm_nt without any device allocation: the library's fixed scratch buffer replaces the
+    per-stream stream-K workspace.  Calls that overlap in time share that buffer and race, so
+    order them; make the first call on each device before capturing any stream."""
+    _need(_is_fp8(A) and A.dim() == 2 and A.stride(1) == 1, "A: e4m3 [M,K]")
+    _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
+    _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
+    _need(sA.dtype == torch.float32 and sB.dtype == torch.float32 and sB.is_contiguous(), "scales: f32")
+    M, K = A.shape
+    N = B.shape[0]
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_gemm_nt_noalloc(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
+                                     _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt_noalloc")
 
 
 def fp8_grouped_gemm_contiguous(A, sA, B, sB, D, group_offsets) -> None:

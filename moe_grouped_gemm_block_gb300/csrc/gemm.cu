@@ -1028,6 +1028,29 @@ bool env_streamk() {
   return !(e && e[0] == '0' && e[1] == 0);
 }
 
+// Fixed scratch of fp8_gemm_nt_noalloc: the stream-K slots of up to kNoAllocSlots SMs, then the
+// flags.  Part of the library's device image, so using it allocates nothing.
+constexpr int kNoAllocSlots = 160;
+constexpr size_t kNoAllocFlagBytes = 1024;
+constexpr size_t kNoAllocBytes = kSkSlotBytes * kNoAllocSlots + kNoAllocFlagBytes;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocDevices = 64;
+std::once_flag g_noalloc_once[kNoAllocDevices];
+void* g_noalloc_addr[kNoAllocDevices] = {};
+
+// Device address of the fixed scratch on device `dev` (the current device), looked up on the
+// first call for that device; null if the lookup failed.
+void* noalloc_scratch(int dev) {
+  if (dev < 0 || dev >= kNoAllocDevices) return nullptr;
+  std::call_once(g_noalloc_once[dev], [dev] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) g_noalloc_addr[dev] = p;
+    else cudaGetLastError();
+  });
+  return g_noalloc_addr[dev];
+}
+
 thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0;
 
 // FP8G_PAIR=1 runs 256-wide tiles as 256 x 256 CTA-pair tiles, FP8G_PAIR=2 as 256 x 128 pair
@@ -1078,7 +1101,7 @@ struct Operands {
 };
 
 template <int MODE>
-int run_gemm(const Operands& o, cudaStream_t stream) {
+int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
   if (st != FP8G_OK) return st;
@@ -1167,7 +1190,17 @@ int run_gemm(const Operands& o, cudaStream_t stream) {
       (MODE == kMasked || tail_splits(a.num_tiles))) {
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    if (sk_workspace(dev_id, dev->sm_count, stream, &a.ws_part, &a.ws_flag)) {
+    bool have_ws = false;
+    if (no_alloc) {  // the fixed scratch (the caller has checked that it holds every SM's slot)
+      void* p = noalloc_scratch(dev_id);
+      if (!p) return FP8G_ERR_CUDA;
+      a.ws_part = static_cast<float4*>(p);
+      a.ws_flag = reinterpret_cast<uint32_t*>(static_cast<char*>(p) + kSkSlotBytes * kNoAllocSlots);
+      have_ws = true;
+    } else {
+      have_ws = sk_workspace(dev_id, dev->sm_count, stream, &a.ws_part, &a.ws_flag);
+    }
+    if (have_ws) {
       if (cudaMemsetAsync(a.ws_flag, 0, static_cast<size_t>(dev->sm_count) * 4, stream) != cudaSuccess) {
         cudaGetLastError();
         return FP8G_ERR_CUDA;
@@ -1237,6 +1270,28 @@ extern "C" int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t 
     return FP8G_ERR_ALIGNMENT;
   Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr};
   return run_gemm<kDense>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_gemm_nt_noalloc(const void* A, int64_t lda, const float* sA, int64_t ld_sa,
+                                   const void* B, int64_t ldb, const float* sB, void* D,
+                                   int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
+  // the argument rules of fp8_gemm_nt
+  if (M < 0 || M > kMaxI32 || N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 ||
+      K > kMaxI32)
+    return FP8G_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldd < N || ld_sa < M) return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;
+  if (!A || !sA || !B || !sB || !D) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0 || ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  // the fixed scratch holds kNoAllocSlots SMs' slots: a larger device is out of its range
+  DeviceInfo* dev = nullptr;
+  const int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  if (dev->sm_count > kNoAllocSlots) return FP8G_ERR_INVALID_ARG;
+  Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr};
+  return run_gemm<kDense>(o, static_cast<cudaStream_t>(stream), true);
 }
 
 extern "C" int fp8_grouped_gemm_contiguous(const void* A, const float* sA, int64_t ld_sa,
