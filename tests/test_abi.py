@@ -108,3 +108,16 @@ def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         g.lib()
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(K=200), INVALID), (dict(N=250), INVALID), (dict(M=-1), INVALID), (dict(ldd=128), INVALID),
+    (dict(A=None), INVALID), (dict(A=P + 1), ALIGN), (dict(lda=264), ALIGN),
+])
+def test_gemm_nt_noalloc_validation(lib, kw, want):
+    # the fixed-scratch variant takes fp8_gemm_nt's arguments and rules
+    assert lib.fp8_gemm_nt_noalloc(*_nt(**kw)) == want
+
+
+def test_gemm_nt_noalloc_m_zero_is_a_noop(lib):
+    assert lib.fp8_gemm_nt_noalloc(*_nt(M=0, A=None, sA=None, B=None, sB=None, D=None)) == 0
