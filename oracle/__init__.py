@@ -15,6 +15,7 @@ Modules:
   quantize  -- 1x128 activation and 128x128 weight block quantisation
   gemm      -- the blockwise-dequantised GEMM with per-K-block promotion, and its
                contiguous / masked grouped MoE forms
+  route     -- the contiguous grouped layout built from routed tokens, gathered and quantised
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 invariants, brute force on tiny inputs and library routines; none is "parity
 unpinned".
@@ -23,9 +24,10 @@ unpinned".
 from .e4m3 import E4M3_MAX, e4m3_decode, e4m3_decode_table, e4m3_encode, bf16_round_bits, bf16_bits_to_f32
 from .quantize import quantize_1x128, quantize_128x128
 from .gemm import gemm_nt, grouped_contiguous, grouped_masked
+from .route import route_gather_quantize, route_layout
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_decode_table", "e4m3_encode", "bf16_round_bits",
     "bf16_bits_to_f32", "quantize_1x128", "quantize_128x128", "gemm_nt", "grouped_contiguous",
-    "grouped_masked",
+    "grouped_masked", "route_gather_quantize", "route_layout",
 ]
