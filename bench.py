@@ -362,6 +362,7 @@ def run_ours(args, world, rank, local, dist):
     roof["share"] = round(top[1] / sum(k[1] for k in kernels), 3)
 
     e2e = measure_e2e(cases, g, dev, max(3, min(args.steps, 20)), dist, world)
+    next_rows = measure_next_rows(names, g, dev, flush, hbm_peak)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -375,6 +376,7 @@ def run_ours(args, world, rank, local, dist):
         "per_workload": breakdown,
         "roofline": roof,
         "e2e": e2e,
+        "next_rows": next_rows,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
@@ -384,6 +386,51 @@ def run_ours(args, world, rank, local, dist):
         out["cpu_baseline"] = cpu_baseline(names, target_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def measure_next_rows(names, g, dev, flush, hbm_peak, reps=20):
+    """Rows beyond the headline step, timed on their own: route-gather-quantize (the contiguous
+    grouped layout built on the device from the MoE contiguous workload's 4096 routed tokens)."""
+    if "moe_contiguous" not in names:
+        return {}
+    w = WORKLOADS["moe_contiguous"]
+    inp = make_inputs(w, dev)
+    x, ids = inp["tokens"], inp["topk_ids"].to(dev)
+    T, K = x.shape
+    m_cap = g.route_capacity(T, w.topk, w.E)
+    q = torch.empty((m_cap, K), dtype=torch.uint8, device=dev)
+    sA = torch.empty((K // 128, m_cap), dtype=torch.float32, device=dev)
+    offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    rows = torch.empty(m_cap, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    lib = g.lib()
+
+    def call():
+        st = lib.fp8_route_gather_quantize_1x128(x.data_ptr(), T, K, K, ids.data_ptr(), w.topk, w.E, q.data_ptr(),
+                                                 K, sA.data_ptr(), m_cap, offs.data_ptr(), rows.data_ptr(), m_cap,
+                                                 stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"route_gather_quantize failed: {g.STATUS.get(st, st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for i in range(3):
+        call()
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if g.fp8g_get_status() != 0:
+        raise RuntimeError("device status not OK after route_gather_quantize")
+    us = statistics.median(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    # algorithmic bytes: each token row read once, the ids, the codes / scales / token map written
+    nbytes = T * K * 2 + ids.numel() * 4 + m_cap * K + m_cap * (K // 128) * 4 + m_cap * 4 + (w.E + 1) * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"route_gather_quantize_1x128": {
+        "workload": f"moe_contiguous routing: {T} tokens x top-{w.topk} of {w.E} experts, K={K}, M_cap={m_cap}",
+        "us": round(us, 2), "gbs": round(gbs, 1), "pct_hbm_peak": round(100 * gbs / hbm_peak, 1),
+        "launches": 2, "note": "median of 20, L2 flushed before each; not part of the headline step"}}
 
 
 def measure_e2e(cases, g, dev, steps, dist, world):

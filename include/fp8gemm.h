@@ -86,6 +86,37 @@ int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, void* q
                        float* sA, int64_t ld_sa, void* stream);
 
 /*
+ * fp8_route_gather_quantize_1x128 -- builds the contiguous grouped layout that
+ * fp8_grouped_gemm_contiguous reads, straight from routed tokens, and quantises it
+ * ("DeepGEMM explainer" sec. 3.2 and 4.2; "DeepGEMM FP8 walk-through" sec. 5.3:
+ * each expert's rows contiguous and block-loadable, described by group offsets).
+ *
+ *   x              bf16 [T, K] tokens, row stride ldx elements (ldx >= K, ldx % 8 == 0)
+ *   topk_ids       int32 [T, topk], DEVICE memory: the experts each token is routed to
+ *   q, sA          outputs as fp8_quantize_1x128 writes them, for M_cap rows:
+ *                  e4m3 [M_cap, K] (row stride ldq bytes) and fp32 [K/128][ld_sa >= M_cap]
+ *   group_offsets  int32 [E+1], DEVICE memory, output: expert e owns rows
+ *                  group_offsets[e] .. group_offsets[e+1]-1 (multiples of 128)
+ *   row_token      int32 [M_cap], DEVICE memory, output: the token of each row, -1 for a
+ *                  padding row
+ *   M_cap          rows of q / sA / row_token: a multiple of 128 and at least
+ *                  T*topk + 127*E (every group padded to 128 fits)
+ *
+ * Inside a group the rows hold the expert's tokens in ascending order (a token that names
+ * one expert twice gets two rows), then zero rows up to the next multiple of 128.  Every
+ * row with token -1 -- padding, and the rows from group_offsets[E] to M_cap -- has scale
+ * 0 and codes 0.  Call the grouped GEMM with M_total = M_cap: rows outside every group
+ * are skipped and their output rows left untouched.  Expert ids outside [0, E) are
+ * dropped and set FP8G_ERR_DEVICE_ASSERT.  T >= 0, topk >= 1, 1 <= E <= 2048,
+ * K % 128 == 0, M_cap * (K/128) < 2^31.  x, q, sA 16-byte aligned (x may be null when
+ * T == 0).
+ */
+int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                    const int32_t* topk_ids, int32_t topk, int32_t E, void* q,
+                                    int64_t ldq, float* sA, int64_t ld_sa, int32_t* group_offsets,
+                                    int32_t* row_token, int64_t M_cap, void* stream);
+
+/*
  * fp8_quantize_128x128 -- weight quantisation, one scale per 128x128 block
  * ("DeepGEMM explainer" sec. 5.1; "DeepGEMM FP8 walk-through" sec. 2.2).
  * Same rule as fp8_quantize_1x128 with amax taken over the block's rows that

@@ -131,9 +131,12 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, bool direc
 constexpr int kQThreads = 256;
 constexpr int kQUnroll = 2;
 
+// GATHER: output row m holds input row row_src[m] (a zero row where row_src[m] < 0).
+template <bool GATHER>
 __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
-    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa) {
+    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa,
+    const int32_t* __restrict__ row_src) {
   const int sub = threadIdx.x & 7;
   const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) >> 3;
   const uint32_t n_groups = gridDim.x * (kQThreads >> 3);
@@ -147,8 +150,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
       m[u] = item / KB;
       kb[u] = item - m[u] * KB;
       raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (item < total) {
-        const __nv_bfloat16* src = x + m[u] * ldx + kb[u] * 128 + sub * 8;
+      int64_t src_row = m[u];
+      if (GATHER && item < total) src_row = __ldg(row_src + m[u]);
+      if (item < total && src_row >= 0) {
+        const __nv_bfloat16* src = x + src_row * ldx + kb[u] * 128 + sub * 8;
         raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
         raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 64));
       }
@@ -225,6 +230,180 @@ __global__ void __launch_bounds__(256) quantize_128x128_kernel(
   if (t == 0) sB[(e * NB + nb) * KB + kb] = s;
 }
 
+// ---------------------------------------------------------------- routing layout
+// One CTA builds the contiguous grouped layout from the expert choices ids[T*k] (token-major):
+// group_offsets[E+1] (each group's row count rounded up to 128) and row_token[M_cap] (the token
+// of each row; -1 for padding rows and for rows past the last group).  Inside a group the rows
+// follow the entries' order, i.e. ascending tokens.  Ids outside [0, E) are dropped and flag
+// FP8G_ERR_DEVICE_ASSERT; if the padded rows would not fit into M_cap, the layout is left empty
+// (all offsets 0) and the same status is raised.
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteMaxExperts = 2048;
+constexpr int kRouteChunk = 4096;  // entries staged in shared memory per pass of the assigning warp
+
+__global__ void __launch_bounds__(kRouteThreads) route_layout_kernel(
+    const int32_t* __restrict__ ids, int32_t n, int32_t topk, int32_t E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_token, int64_t M_cap, unsigned int* status) {
+  __shared__ int32_t s_count[kRouteMaxExperts];     // per-expert counts, then running ranks
+  __shared__ int32_t s_off[kRouteMaxExperts + 1];   // padded prefix
+  __shared__ int32_t s_chunk[kRouteChunk];
+  __shared__ int32_t s_warp[kRouteThreads / 32];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kRouteThreads) s_count[e] = 0;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int32_t i = tid; i < n; i += kRouteThreads) {
+    const int32_t e = __ldg(ids + i);
+    if (e >= 0 && e < E) atomicAdd(&s_count[e], 1);
+    else s_bad = 1;
+  }
+  __syncthreads();
+  // exclusive scan of the padded counts: thread tid covers experts [tid*per, tid*per + per)
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  int32_t local = 0;
+  for (int j = 0; j < per; ++j) {
+    const int e = tid * per + j;
+    if (e < E) local += (s_count[e] + 127) / 128 * 128;
+  }
+  int32_t incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = s_warp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += v;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t run = (warp > 0 ? s_warp[warp - 1] : 0) + incl - local;  // exclusive start of this thread
+  for (int j = 0; j < per; ++j) {
+    const int e = tid * per + j;
+    if (e < E) {
+      s_off[e] = run;
+      run += (s_count[e] + 127) / 128 * 128;
+    }
+  }
+  if (tid == kRouteThreads - 1) s_off[E] = s_warp[31];
+  __syncthreads();
+  const bool fits = static_cast<int64_t>(s_off[E]) <= M_cap;
+  for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = fits ? s_off[e] : 0;
+  for (int64_t r = tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
+  for (int e = tid; e < E; e += kRouteThreads) s_count[e] = 0;  // now: rows handed out per expert
+  __syncthreads();
+  // rows in entry order: one warp walks the entries 32 at a time; lanes choosing the same expert
+  // take consecutive rows in lane order (match_any), the last of them advances the expert's count
+  for (int32_t c0 = 0; fits && c0 < n; c0 += kRouteChunk) {
+    const int32_t cn = n - c0 < kRouteChunk ? n - c0 : kRouteChunk;
+    for (int32_t i = tid; i < cn; i += kRouteThreads) s_chunk[i] = __ldg(ids + c0 + i);
+    __syncthreads();
+    if (warp == 0) {
+      for (int32_t b = 0; b < cn; b += 32) {
+        const int32_t i = b + lane;
+        int32_t e = i < cn ? s_chunk[i] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0) row_token[s_off[e] + s_count[e] + rank] = (c0 + i) / topk;
+        __syncwarp();
+        if (e >= 0 && (peers >> lane) == 1u) s_count[e] += __popc(peers);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0 && (s_bad || !fits)) record_status(status, FP8G_ERR_DEVICE_ASSERT);
+}
+
+// The same layout for E <= 256 with all 32 warps assigning rows: warp w takes the contiguous
+// entry range [w*L, (w+1)*L) and keeps its own per-expert counts; an exclusive scan over the
+// warps gives each warp its first row per expert, so rows still follow the entries' order.
+constexpr int kRouteSmallExperts = 256;
+
+__global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
+    const int32_t* __restrict__ ids, int32_t n, int32_t topk, int32_t E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_token, int64_t M_cap, unsigned int* status) {
+  constexpr int W = kRouteThreads / 32;
+  __shared__ int32_t s_wcnt[W][kRouteSmallExperts];  // counts, then each warp's first rank
+  __shared__ int32_t s_off[kRouteSmallExperts + 1];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < W * kRouteSmallExperts; i += kRouteThreads) (&s_wcnt[0][0])[i] = 0;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  const int32_t L = (n + W - 1) / W;
+  const int32_t lo = warp * L, hi = min(n, lo + L);
+  for (int32_t i = lo + lane; i < hi; i += 32) {
+    const int32_t e = __ldg(ids + i);
+    if (e >= 0 && e < E) atomicAdd(&s_wcnt[warp][e], 1);
+    else s_bad = 1;
+  }
+  __syncthreads();
+  if (tid < E) {  // per expert: exclusive scan over the warps, total in s_off (temporarily)
+    int32_t run = 0;
+    for (int w = 0; w < W; ++w) {
+      const int32_t c = s_wcnt[w][tid];
+      s_wcnt[w][tid] = run;
+      run += c;
+    }
+    s_off[tid] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {  // padded counts -> exclusive prefix (8 experts per lane)
+    int32_t v[kRouteSmallExperts / 32];
+    int32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < kRouteSmallExperts / 32; ++j) {
+      const int e = lane * (kRouteSmallExperts / 32) + j;
+      v[j] = e < E ? (s_off[e] + 127) / 128 * 128 : 0;
+      local += v[j];
+    }
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += u;
+    }
+    int32_t run = incl - local;
+    const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kRouteSmallExperts / 32; ++j) {
+      const int e = lane * (kRouteSmallExperts / 32) + j;
+      if (e < E) s_off[e] = run;
+      run += v[j];
+    }
+    if (lane == 0) s_off[E] = total;
+  }
+  __syncthreads();
+  const bool fits = static_cast<int64_t>(s_off[E]) <= M_cap;
+  for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = fits ? s_off[e] : 0;
+  for (int64_t r = tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
+  __syncthreads();
+  if (fits) {
+    for (int32_t b = lo; b < hi; b += 32) {
+      const int32_t i = b + lane;
+      int32_t e = i < hi ? __ldg(ids + i) : -1;
+      if (e < 0 || e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (e >= 0) row_token[s_off[e] + s_wcnt[warp][e] + rank] = i / topk;
+      __syncwarp();
+      if (e >= 0 && (peers >> lane) == 1u) s_wcnt[warp][e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  if (tid == 0 && (s_bad || !fits)) record_status(status, FP8G_ERR_DEVICE_ASSERT);
+}
+
 }  // namespace
 }  // namespace fp8g
 
@@ -248,10 +427,50 @@ extern "C" int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t l
   int64_t blocks = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
   if (blocks > cap) blocks = cap;
-  quantize_1x128_kernel<<<static_cast<unsigned>(blocks), kQThreads, 0,
-                          static_cast<cudaStream_t>(stream)>>>(
+  quantize_1x128_kernel<false><<<static_cast<unsigned>(blocks), kQThreads, 0,
+                                 static_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx,
-      static_cast<uint8_t*>(q), ldq, sA, ld_sa);
+      static_cast<uint8_t*>(q), ldq, sA, ld_sa, nullptr);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                               const int32_t* topk_ids, int32_t topk, int32_t E,
+                                               void* q, int64_t ldq, float* sA, int64_t ld_sa,
+                                               int32_t* group_offsets, int32_t* row_token,
+                                               int64_t M_cap, void* stream) {
+  if (T < 0 || T > 0x7FFFFFFF || K <= 0 || K % 128 != 0 || topk < 1 || E < 1 ||
+      E > kRouteMaxExperts || ldx < K || ldq < K)
+    return FP8G_ERR_INVALID_ARG;
+  const int64_t n = T * topk;
+  if (n > 0x7FFFFFFF || M_cap % 128 != 0 || M_cap < n + int64_t{127} * E || ld_sa < M_cap ||
+      M_cap * (K / 128) >= (int64_t{1} << 31))
+    return FP8G_ERR_INVALID_ARG;
+  if (!q || !sA || !group_offsets || !row_token || (n > 0 && (!x || !topk_ids)))
+    return FP8G_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || !aligned16(q) || !aligned16(sA) || ldx % 8 != 0 || ldq % 16 != 0 ||
+      ld_sa % 4 != 0 || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(group_offsets) & 3u) || (reinterpret_cast<uintptr_t>(row_token) & 3u))
+    return FP8G_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (E <= kRouteSmallExperts)
+    route_layout_small_kernel<<<1, kRouteThreads, 0, s>>>(topk_ids, static_cast<int32_t>(n), topk, E,
+                                                          group_offsets, row_token, M_cap, dev->status);
+  else
+    route_layout_kernel<<<1, kRouteThreads, 0, s>>>(topk_ids, static_cast<int32_t>(n), topk, E, group_offsets,
+                                                    row_token, M_cap, dev->status);
+  if (cudaGetLastError() != cudaSuccess) return FP8G_ERR_CUDA;
+  const int64_t items = M_cap * (K / 128);
+  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  int64_t blocks = (items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
+  if (blocks > cap) blocks = cap;
+  quantize_1x128_kernel<true><<<static_cast<unsigned>(blocks), kQThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M_cap), static_cast<uint32_t>(K / 128), ldx,
+      static_cast<uint8_t*>(q), ldq, sA, ld_sa, row_token);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

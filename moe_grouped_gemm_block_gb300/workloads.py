@@ -133,8 +133,9 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     """Draw the bf16 inputs of workload ``w`` on ``device``.
 
     Keys: "A" (bf16, [M,K] / [M_total,K] / [E,cap,K]), "B" (bf16 [N,K] or
-    [E,N,K]); contiguous adds "group_offsets" (int32 [E+1], CPU) and
-    "row_token"; masked adds "masked_m" (int32 [E], CPU).
+    [E,N,K]); contiguous adds "group_offsets" (int32 [E+1], CPU), "row_token",
+    and the unrouted "tokens" (bf16 [T,K]) with their "topk_ids" (int32 [T,topk],
+    CPU); masked adds "masked_m" (int32 [E], CPU).
     """
     device = torch.device(device)
     g = _gen(w.seed, device)
@@ -159,7 +160,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         A = torch.zeros((row_token.numel(), w.K), dtype=torch.bfloat16, device=device)
         valid = (row_token >= 0).nonzero().squeeze(1)
         A[valid.to(device)] = x[row_token[valid].to(device)]
-        out.update(A=A, B=B, group_offsets=offsets, row_token=row_token)
+        out.update(A=A, B=B, group_offsets=offsets, row_token=row_token, tokens=x,
+                   topk_ids=exp_of.reshape(w.tokens, w.topk).to(torch.int32))
     elif w.kind == "masked":
         a32 = _normal((w.E, w.cap, w.K), 1.0, g, device)
         B = _weights(w, g, device)
