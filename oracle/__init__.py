@@ -16,6 +16,8 @@ Modules:
   gemm      -- the blockwise-dequantised GEMM with per-K-block promotion, and its
                contiguous / masked grouped MoE forms
   route     -- the contiguous grouped layout built from routed tokens, gathered and quantised
+  scaled    -- per-tensor / per-token / per-channel quantisation and the GEMM that applies
+               those scales once, in the epilogue, with its grouped forms
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 invariants, brute force on tiny inputs and library routines; none is "parity
 unpinned".
@@ -25,9 +27,12 @@ from .e4m3 import E4M3_MAX, e4m3_decode, e4m3_decode_table, e4m3_encode, bf16_ro
 from .quantize import quantize_1x128, quantize_128x128
 from .gemm import gemm_nt, grouped_contiguous, grouped_masked
 from .route import route_gather_quantize, route_layout
+from .scaled import (gemm_nt_scaled, grouped_contiguous_scaled, grouped_masked_scaled, quantize_per_row,
+                     quantize_per_tensor)
 
 __all__ = [
     "E4M3_MAX", "e4m3_decode", "e4m3_decode_table", "e4m3_encode", "bf16_round_bits",
     "bf16_bits_to_f32", "quantize_1x128", "quantize_128x128", "gemm_nt", "grouped_contiguous",
-    "grouped_masked", "route_gather_quantize", "route_layout",
+    "grouped_masked", "route_gather_quantize", "route_layout", "gemm_nt_scaled",
+    "grouped_contiguous_scaled", "grouped_masked_scaled", "quantize_per_row", "quantize_per_tensor",
 ]
