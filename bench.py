@@ -362,7 +362,7 @@ def run_ours(args, world, rank, local, dist):
     roof["share"] = round(top[1] / sum(k[1] for k in kernels), 3)
 
     e2e = measure_e2e(cases, g, dev, max(3, min(args.steps, 20)), dist, world)
-    next_rows = measure_next_rows(names, g, dev, flush, hbm_peak)
+    next_rows = measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -388,11 +388,31 @@ def run_ours(args, world, rank, local, dist):
         print(json.dumps(out), flush=True)
 
 
-def measure_next_rows(names, g, dev, flush, hbm_peak, reps=20):
-    """Rows beyond the headline step, timed on their own: route-gather-quantize (the contiguous
-    grouped layout built on the device from the MoE contiguous workload's 4096 routed tokens)."""
+def _time_calls(call, flush, reps=20, warm=3):
+    """Median device time (us) of `call` on the current stream, L2 flushed before each."""
+    stream = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for _ in range(warm):
+        call()
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+
+
+def measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak, reps=20):
+    """Rows beyond the headline step, each timed on its own (median of `reps`, L2 flushed before
+    each): route-gather-quantize (the contiguous grouped layout built on the device from the MoE
+    contiguous workload's 4096 routed tokens); the per-token / per-channel and per-tensor scaled
+    GEMMs and their quantisers on the 4096 x 8192 x 8192 shape and the MoE contiguous workload."""
+    out = {}
+    if "large_4096x8192" in names:
+        out.update(measure_scaled_rows(g, dev, flush, hbm_peak, fp8_peak, reps))
     if "moe_contiguous" not in names:
-        return {}
+        return out
     w = WORKLOADS["moe_contiguous"]
     inp = make_inputs(w, dev)
     x, ids = inp["tokens"], inp["topk_ids"].to(dev)
@@ -427,10 +447,60 @@ def measure_next_rows(names, g, dev, flush, hbm_peak, reps=20):
     # algorithmic bytes: each token row read once, the ids, the codes / scales / token map written
     nbytes = T * K * 2 + ids.numel() * 4 + m_cap * K + m_cap * (K // 128) * 4 + m_cap * 4 + (w.E + 1) * 4
     gbs = nbytes / (us * 1e-6) / 1e9
-    return {"route_gather_quantize_1x128": {
+    out["route_gather_quantize_1x128"] = {
         "workload": f"moe_contiguous routing: {T} tokens x top-{w.topk} of {w.E} experts, K={K}, M_cap={m_cap}",
         "us": round(us, 2), "gbs": round(gbs, 1), "pct_hbm_peak": round(100 * gbs / hbm_peak, 1),
-        "launches": 2, "note": "median of 20, L2 flushed before each; not part of the headline step"}}
+        "launches": 2, "note": "median of 20, L2 flushed before each; not part of the headline step"}
+    # per-token x per-channel grouped GEMM on the same workload's contiguous layout
+    A, B = inp["A"], inp["B"]
+    E, N, _ = B.shape
+    offs = inp["group_offsets"].to(dev)
+    qa, sa = g.quantize_per_row(A)
+    qb, sb = g.quantize_per_row(B.reshape(E * N, K))
+    qb = qb.reshape(E, N, K)
+    D = torch.empty((A.shape[0], N), dtype=torch.bfloat16, device=dev)
+    us = _time_calls(lambda: g.fp8_grouped_gemm_contiguous_scaled(qa, sa, qb, sb, D, offs), flush, reps)
+    flops = 2.0 * T * w.topk * N * K
+    tf = flops / (us * 1e-6) / 1e12
+    out["grouped_gemm_contiguous_scaled"] = {
+        "workload": f"moe_contiguous, per-token A x per-channel B: M_total={A.shape[0]}, E={E}, N={N}, K={K}",
+        "us": round(us, 2), "tflops": round(tf, 1), "pct_fp8_peak": round(100 * tf / fp8_peak, 1), "launches": 1}
+    del qa, qb, D
+    return out
+
+
+def measure_scaled_rows(g, dev, flush, hbm_peak, fp8_peak, reps):
+    """The epilogue-scaled GEMM (per-token x per-channel, and per-tensor) and its quantisers on the
+    4096 x 8192 x 8192 workload's inputs."""
+    w = WORKLOADS["large_4096x8192"]
+    inp = make_inputs(w, dev)
+    A, B = inp["A"], inp["B"]
+    M, K = A.shape
+    N = B.shape[0]
+    out = {}
+    qa, sa = g.quantize_per_row(A)
+    qb, sb = g.quantize_per_row(B)
+    qa_t, sa_t = g.quantize_per_tensor(A)
+    qb_t, sb_t = g.quantize_per_tensor(B)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flops = 2.0 * M * N * K
+    for key, args in (("gemm_nt_scaled_per_channel", (qa, sa, qb, sb)),
+                      ("gemm_nt_scaled_per_tensor", (qa_t, sa_t, qb_t, sb_t))):
+        us = _time_calls(lambda: g.fp8_gemm_nt_scaled(*args, D), flush, reps)
+        tf = flops / (us * 1e-6) / 1e12
+        out[key] = {"workload": f"large_4096x8192: M={M}, N={N}, K={K}", "us": round(us, 2),
+                    "tflops": round(tf, 1), "pct_fp8_peak": round(100 * tf / fp8_peak, 1), "launches": 1,
+                    "config": g.fp8g_last_config()}
+    qbytes = M * K * 3 + M * 4  # bf16 read, e4m3 written, scales
+    for key, fn, launches in (("quantize_per_row", lambda: g.fp8_quantize_per_row(A, qa, sa), 1),
+                              ("quantize_per_tensor", lambda: g.fp8_quantize_per_tensor(A, qa_t, sa_t), 2)):
+        us = _time_calls(fn, flush, reps)
+        gbs = qbytes / (us * 1e-6) / 1e9
+        out[key] = {"workload": f"A of large_4096x8192: {M} x {K} bf16", "us": round(us, 2), "gbs": round(gbs, 1),
+                    "pct_hbm_peak": round(100 * gbs / hbm_peak, 1), "launches": launches}
+    if g.fp8g_get_status() != 0:
+        raise RuntimeError("device status not OK after the scaled rows")
+    return out
 
 
 def measure_e2e(cases, g, dev, steps, dist, world):

@@ -222,6 +222,79 @@ int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t ld_sa, const
                             int64_t cap, int64_t N, int64_t K, void* stream);
 
 /*
+ * Per-tensor / per-token / per-channel scales ("DeepGEMM FP8 walk-through" sec. 2.2:
+ * one scale for a whole tensor, or one per token of A and one per output channel of B;
+ * "Production FP8 GEMM alignment and Tensor Core peak tuning", the Triton listing's
+ * fused epilogue: the FP32 accumulator of the whole K is multiplied once by
+ * scale_a * scale_b, then converted to BF16).  Same scale and code rule as the block
+ * forms, with the group a whole row or the whole tensor:
+ *     amax = max |x|;  s = fp32(amax / 448);  q = e4m3(fp32(x / s));  amax == 0: s = 0, codes 0.
+ */
+
+/*
+ * fp8_quantize_per_row -- one scale per row over the whole K (per-token for
+ * activations, per-channel for weights [N, K] or [E*N, K]).
+ *
+ *   x   bf16 [M, K], row stride ldx elements (ldx >= K, ldx % 8 == 0)
+ *   q   e4m3 [M, K], row stride ldq bytes (ldq >= K, ldq % 16 == 0)
+ *   s   fp32 [M]
+ *   M >= 0 (M == 0: no-op), K > 0, K % 128 == 0.  x, q 16-byte aligned, s 4-byte aligned.
+ */
+int fp8_quantize_per_row(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                         float* s, void* stream);
+
+/*
+ * fp8_quantize_per_tensor -- one scale per tensor, for E tensors of M rows each (E = 1 for
+ * activations; E experts' weights).  Tensor e is rows e*M .. e*M+M-1 of x and q.
+ *
+ *   x   bf16 [E*M, K], row stride ldx elements (ldx >= K, ldx % 8 == 0)
+ *   q   e4m3 [E*M, K], row stride ldq bytes (ldq >= K, ldq % 16 == 0)
+ *   s   fp32 [E], output (an empty tensor, M == 0, gets s = 0)
+ *   1 <= E <= 65535, M >= 0, K % 128 == 0, M * K / 8 < 2^31.  x, q 16-byte aligned, s 4-byte
+ *   aligned.  Two passes over x (the second mostly from L2 when a tensor fits it) and a
+ *   memset of s, all on `stream`.
+ */
+int fp8_quantize_per_tensor(const void* x, int64_t E, int64_t M, int64_t K, int64_t ldx, void* q,
+                            int64_t ldq, float* s, void* stream);
+
+/*
+ * fp8_gemm_nt_scaled -- dense D = bf16(fp32(acc) * fp32(sA[m] * sB[n])), acc[m, n] the FP32
+ * sum over the whole K of A[m, k] * B[n, k].
+ *
+ *   A, lda, B, ldb, D, ldd, M, N, K   as fp8_gemm_nt
+ *   sA   sa_per_row = 1: fp32 [M], one scale per row of A; 0: fp32 [1], one for all of A
+ *   sB   sb_per_col = 1: fp32 [N], one scale per row of B (column of D), 16-byte aligned;
+ *        0: fp32 [1]
+ *   sa_per_row, sb_per_col in {0, 1}.  sA (and sB when sb_per_col == 0) 4-byte aligned.
+ * Uses the stream-K workspace of "GEMM workspace" above.
+ */
+int fp8_gemm_nt_scaled(const void* A, int64_t lda, const float* sA, int32_t sa_per_row,
+                       const void* B, int64_t ldb, const float* sB, int32_t sb_per_col, void* D,
+                       int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * fp8_grouped_gemm_contiguous_scaled -- fp8_grouped_gemm_contiguous with epilogue scales:
+ *   sA   sa_per_row = 1: fp32 [M_total] (row of A); 0: fp32 [1]
+ *   sB   sb_per_col = 1: fp32 [E][N] (16-byte aligned); 0: fp32 [E], one per expert
+ * Other arguments, layout and errors as fp8_grouped_gemm_contiguous.
+ */
+int fp8_grouped_gemm_contiguous_scaled(const void* A, const float* sA, int32_t sa_per_row,
+                                       const void* B, const float* sB, int32_t sb_per_col,
+                                       void* D, const int32_t* group_offsets, int32_t E,
+                                       int64_t M_total, int64_t N, int64_t K, void* stream);
+
+/*
+ * fp8_grouped_gemm_masked_scaled -- fp8_grouped_gemm_masked with epilogue scales:
+ *   sA   sa_per_row = 1: fp32 [E*cap], row index e*cap + m; 0: fp32 [1]
+ *   sB   sb_per_col = 1: fp32 [E][N] (16-byte aligned); 0: fp32 [E]
+ * Other arguments, layout and errors as fp8_grouped_gemm_masked.
+ */
+int fp8_grouped_gemm_masked_scaled(const void* A, const float* sA, int32_t sa_per_row,
+                                   const void* B, const float* sB, int32_t sb_per_col, void* D,
+                                   const int32_t* masked_m, int32_t E, int64_t cap, int64_t N,
+                                   int64_t K, void* stream);
+
+/*
  * fp8g_get_status -- synchronise `stream`, then return and clear the current
  * device's status word (FP8G_OK if no kernel recorded an error since the last
  * call).  Returns FP8G_ERR_CUDA if the synchronisation itself fails.

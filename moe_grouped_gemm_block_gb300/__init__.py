@@ -9,6 +9,11 @@ functions here carry the same names and take torch tensors:
     fp8_gemm_nt(A, sA, B, sB, D)                      D bf16 [M,N] = A [M,K] x B [N,K]^T with block scales
     fp8_grouped_gemm_contiguous(A, sA, B, sB, D, group_offsets)
     fp8_grouped_gemm_masked(A, sA, B, sB, D, masked_m)
+    fp8_route_gather_quantize_1x128 (see route_gather_quantize_1x128)
+    fp8_quantize_per_row(x, q, s) / fp8_quantize_per_tensor(x, q, s)   one scale per row / per tensor
+    fp8_gemm_nt_scaled(A, sA, B, sB, D)                  epilogue scales: sA [M] or [1], sB [N] or [1]
+    fp8_grouped_gemm_contiguous_scaled(A, sA, B, sB, D, group_offsets)   sB [E,N] or [E]
+    fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m)
 
 e4m3 tensors may be torch.uint8 or torch.float8_e4m3fn.  Work is enqueued on the
 current CUDA stream of the tensors' device.  A non-zero status raises Fp8GemmError.
@@ -53,6 +58,11 @@ _SIGNATURES = {
                                         _I64, _P],
     "fp8_grouped_gemm_contiguous": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_masked": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8_quantize_per_row": [_P, _I64, _I64, _I64, _P, _I64, _FP, _P],
+    "fp8_quantize_per_tensor": [_P, _I64, _I64, _I64, _I64, _P, _I64, _FP, _P],
+    "fp8_gemm_nt_scaled": [_P, _I64, _FP, _I32, _P, _I64, _FP, _I32, _P, _I64, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_contiguous_scaled": [_P, _FP, _I32, _P, _FP, _I32, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_masked_scaled": [_P, _FP, _I32, _P, _FP, _I32, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8g_get_status": [_P],
     "fp8g_last_config": [ctypes.POINTER(ctypes.c_int)] * 3,
 }
@@ -185,6 +195,72 @@ def fp8_grouped_gemm_masked(A, sA, B, sB, D, masked_m) -> None:
            "fp8_grouped_gemm_masked")
 
 
+def fp8_quantize_per_row(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor) -> None:
+    _need(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1, "x: bf16 [M,K], K contiguous")
+    _need(_is_fp8(q) and q.shape == x.shape and q.stride(1) == 1, "q: e4m3 [M,K]")
+    M, K = x.shape
+    _need(s.dtype == torch.float32 and s.is_contiguous() and s.numel() == M, "s: f32 [M]")
+    _check(lib().fp8_quantize_per_row(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream(x)),
+           "fp8_quantize_per_row")
+
+
+def fp8_quantize_per_tensor(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor) -> None:
+    """x bf16 [M,K] (one tensor) or [E,M,K] (E tensors, each its own scale) -> q, s f32 [E]."""
+    _need(x.dtype == torch.bfloat16 and x.dim() in (2, 3) and x.is_contiguous(), "x: bf16 [(E,) M, K] contiguous")
+    _need(_is_fp8(q) and q.shape == x.shape and q.is_contiguous(), "q: e4m3, same shape as x")
+    E, M, K = (1, *x.shape) if x.dim() == 2 else x.shape
+    _need(s.dtype == torch.float32 and s.is_contiguous() and s.numel() == E, "s: f32 [E]")
+    _check(lib().fp8_quantize_per_tensor(_ptr(x), E, M, K, K, _ptr(q), K, _ptr(s), _stream(x)),
+           "fp8_quantize_per_tensor")
+
+
+def _epi_scale(t: torch.Tensor, n: int, what: str) -> int:
+    """1 when t holds one scale per row / column (n of them), 0 when it holds one."""
+    _need(t.dtype == torch.float32 and t.is_contiguous() and t.numel() in (1, n), f"{what}: f32 [{n}] or [1]")
+    return 1 if t.numel() == n and n != 1 else 0
+
+
+def fp8_gemm_nt_scaled(A, sA, B, sB, D) -> None:
+    _need(_is_fp8(A) and A.dim() == 2 and A.stride(1) == 1, "A: e4m3 [M,K]")
+    _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
+    _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
+    M, K = A.shape
+    N = B.shape[0]
+    pa, pb = _epi_scale(sA, M, "sA"), _epi_scale(sB, N, "sB")
+    _check(lib().fp8_gemm_nt_scaled(_ptr(A), A.stride(0), _ptr(sA), pa, _ptr(B), B.stride(0), _ptr(sB), pb,
+                                    _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt_scaled")
+
+
+def fp8_grouped_gemm_contiguous_scaled(A, sA, B, sB, D, group_offsets) -> None:
+    _need(_is_fp8(A) and A.dim() == 2 and A.is_contiguous(), "A: e4m3 [M_total,K] contiguous")
+    _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
+    _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [M_total,N] contiguous")
+    _need(group_offsets.dtype == torch.int32 and group_offsets.is_cuda, "group_offsets: int32 device tensor")
+    M_total, K = A.shape
+    E, N, _ = B.shape
+    pa = _epi_scale(sA, M_total, "sA")
+    _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() in (E, E * N), "sB: f32 [E,N] or [E]")
+    pb = 1 if sB.numel() == E * N and N != 1 else 0
+    _check(lib().fp8_grouped_gemm_contiguous_scaled(_ptr(A), _ptr(sA), pa, _ptr(B), _ptr(sB), pb, _ptr(D),
+                                                    _ptr(group_offsets), E, M_total, N, K, _stream(A)),
+           "fp8_grouped_gemm_contiguous_scaled")
+
+
+def fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m) -> None:
+    _need(_is_fp8(A) and A.dim() == 3 and A.is_contiguous(), "A: e4m3 [E,cap,K] contiguous")
+    _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
+    _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [E,cap,N] contiguous")
+    _need(masked_m.dtype == torch.int32 and masked_m.is_cuda, "masked_m: int32 device tensor")
+    E, cap, K = A.shape
+    N = B.shape[1]
+    pa = _epi_scale(sA, E * cap, "sA")
+    _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() in (E, E * N), "sB: f32 [E,N] or [E]")
+    pb = 1 if sB.numel() == E * N and N != 1 else 0
+    _check(lib().fp8_grouped_gemm_masked_scaled(_ptr(A), _ptr(sA), pa, _ptr(B), _ptr(sB), pb, _ptr(D),
+                                                _ptr(masked_m), E, cap, N, K, _stream(A)),
+           "fp8_grouped_gemm_masked_scaled")
+
+
 def fp8g_get_status(stream: torch.cuda.Stream | None = None) -> int:
     s = (stream or torch.cuda.current_stream()).cuda_stream
     return lib().fp8g_get_status(s)
@@ -248,4 +324,26 @@ def quantize_128x128(w: torch.Tensor):
 def gemm_nt(A, sA, B, sB) -> torch.Tensor:
     D = torch.empty((A.shape[0], B.shape[0]), dtype=torch.bfloat16, device=A.device)
     fp8_gemm_nt(A, sA, B, sB, D)
+    return D
+
+
+def quantize_per_row(x: torch.Tensor):
+    """bf16 [M,K] -> (q uint8 [M,K], s f32 [M]): per-token (activations) or per-channel (weights)."""
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    s = torch.empty(x.shape[0], dtype=torch.float32, device=x.device)
+    fp8_quantize_per_row(x, q, s)
+    return q, s
+
+
+def quantize_per_tensor(x: torch.Tensor):
+    """bf16 [M,K] -> (q, s f32 [1]); bf16 [E,M,K] -> (q, s f32 [E]), one scale per tensor."""
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    s = torch.empty(1 if x.dim() == 2 else x.shape[0], dtype=torch.float32, device=x.device)
+    fp8_quantize_per_tensor(x, q, s)
+    return q, s
+
+
+def gemm_nt_scaled(A, sA, B, sB) -> torch.Tensor:
+    D = torch.empty((A.shape[0], B.shape[0]), dtype=torch.bfloat16, device=A.device)
+    fp8_gemm_nt_scaled(A, sA, B, sB, D)
     return D

@@ -22,6 +22,12 @@
 //                 last K block: BF16, staged in shared memory, stored with TMA (64-byte
 //                 swizzled 32 x 32 boxes).  Rows past a masked expert's count are never
 //                 written.  Narrow tiles (BN = 64) split the K blocks between two warpgroups.
+// Epilogue-scaled variant (EPI; per-tensor / per-token / per-channel scales, "DeepGEMM FP8
+// walk-through" sec. 2.2, the fused epilogue of the Triton listing on "Production FP8 GEMM
+// alignment and Tensor Core peak tuning"): the MMAs of all K blocks of a tile accumulate in
+// place in one TMEM buffer (2 at BN = 256: the epilogue of one tile overlaps the MMAs of the
+// next), each K block's commit frees its stage, and the epilogue reads the accumulator once and
+// multiplies it by sa[m] * sb[n] before the BF16 store.
 // Every wait is bounded: a wait that runs past its cycle budget records FP8G_ERR_TIMEOUT in
 // the status word, raises a shared abort flag, and every role returns.
 
@@ -125,6 +131,9 @@ struct GemmArgs {
   const int32_t* groups;  // contiguous: offsets [E+1]; masked: counts [E]
   unsigned int* status;
   long long budget;
+  // epilogue scaling: sA holds one scale per row of A (sa_step 1) or one for all rows (0); sB one
+  // per column of each expert, [E][N] (sb_step 1), or one per expert, [E] (0)
+  int32_t sa_step, sb_step;
   // stream-K tail (see make_work): on/off, its minimum K blocks per CTA, and the workspace of
   // FP32 partial tiles (one slot per CTA) with one ready flag per CTA (zeroed before the launch)
   int32_t sk;
@@ -364,12 +373,14 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* f, const GemmArgs& a, 
   return true;
 }
 
-template <int BN, int MODE, bool PAIR = false>
+template <int BN, int MODE, bool PAIR = false, bool EPI = false>
 __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD,
                     const GemmArgs a) {
   using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
+  static_assert(!EPI || (C::kKSplit == 1 && C::kMmaWarps == 1 && !PAIR),
+                "epilogue scaling: one K part, one issuer, single-CTA tiles");
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_u32(smem);
@@ -574,7 +585,42 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       // 14-bit start-address field (shared addresses stay below 2^18, so it cannot carry)
       const uint64_t adesc0 = smem_desc_k_sw128(base + C::kOffA);
       const uint64_t bdesc0 = smem_desc_k_sw128(base + C::kOffB);
-      if constexpr (!kLone) {
+      if constexpr (EPI) {
+        // one TMEM accumulator per piece, all its K blocks accumulated in place; the commit after
+        // a K block's MMAs frees its stage, the commit after the last one hands the buffer over
+        uint32_t it = 0, np = 0;
+        bool ok = true;
+        Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+        Piece pc;
+        while (ok && next_piece(w, pc)) {
+          Tile ti;
+          if (!fetch_tile(pc.t, ti)) continue;
+          const uint32_t b = np % NB, tph = (np / NB) & 1u;
+          ++np;
+          if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * BN;
+          for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
+            const uint32_t s = it % S, ph = (it / S) & 1u;
+            if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ad = adesc0 + ((s * C::kStageABytes) >> 4);
+            const uint64_t bd = bdesc0 + ((s * C::kStageBBytes) >> 4);
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              mma_f8f6f4(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > pc.kb0 || k > 0) ? 1u : 0u);
+            mma_commit(leader, empty(s));
+          }
+          if (!ok) break;
+          mma_commit(leader, tfull(b));
+        }
+        if (!ok && it > 0 && leader) {  // the last stage commit completes after every issued MMA
+          const uint32_t last = it - 1;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(empty(last % S), (last / S) & 1u) && clock64() - t0 < a.budget) {
+          }
+        }
+      } else if constexpr (!kLone) {
         uint32_t it = 0;
         bool ok = true;
         Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
@@ -686,7 +732,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     // one issuer: one lane per K part frees the operand stage of each K block once its MMAs
     // are done (the tile's K blocks map one to one onto stages)
     const bool stage_releaser =
-        C::kMmaWarps == 1 && !PAIR && lane == 0 && ew == kpart * 4 * C::kColGroups;
+        !EPI && C::kMmaWarps == 1 && !PAIR && lane == 0 && ew == kpart * 4 * C::kColGroups;
     // this warp's TMEM buffers are released on rank 0's barrier (its own CTA unless paired)
     auto release_tmem = [&](uint32_t b) {
       if (lane == 0) {
@@ -697,6 +743,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     const uint32_t out_addr = base + C::kOffOut + (ew % C::kStoreWarps) * C::kOutBytes;
     float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
     uint32_t it_base = 0, tiles_done = 0;
+    uint32_t np = 0;  // pieces taken (EPI: the TMEM buffer sequence, as the MMA warp counts it)
     bool ok = true;
     // stream-K workspace slot of this thread: float4 j of thread e sits at slot[j * kEpiThreads + e]
     constexpr int kEpiThreads = C::kEpiWarps * 32;
@@ -711,67 +758,88 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       const bool has_cols = ncol0 < a.N;
       // small-M tiles: warps whose rows are all past M skip the promotion (nothing to store)
       const bool live = (MODE != kDenseSmallM && !PAIR) || q * 32 < ti.rows;
-      const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
-      // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
-      // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
-      int32_t sb_base = pc.kb0 & ~31;
-      float sb_cur = (has_cols && sb_base + lane < a.KB) ? ld_nc_f32(sbp + sb_base + lane) : 0.0f;
-      float sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
-      // A-row scale of this thread's row, read from global memory kSAAhead K-block steps
-      // before use (coalesced: a warp reads 32 consecutive rows of one K block)
       const int32_t grow = ti.a_row + row;
       const bool row_ok = grow < a.rows;
-      const float* sap = a.sA + grow;
-      float sa_q[kSAAhead];
-#pragma unroll
-      for (int i = 0; i < kSAAhead; ++i) {
-        const int32_t kbi = pc.kb0 + kpart + i * C::kKSplit;
-        sa_q[i] = (row_ok && kbi < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbi) * a.ld_sa) : 0.0f;
-      }
       float2 acc[C::kEpiCols / 2];
-#pragma unroll
-      for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-      for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += C::kKSplit) {
-        const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
-        const uint32_t b = it % NB, tph = (it / NB) & 1u;
-        const float sa_kb = sa_q[0];
-#pragma unroll
-        for (int i = 0; i + 1 < kSAAhead; ++i) sa_q[i] = sa_q[i + 1];
-        {
-          const int32_t kbn = kb + kSAAhead * C::kKSplit;
-          sa_q[kSAAhead - 1] =
-              (row_ok && kbn < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbn) * a.ld_sa) : 0.0f;
-        }
-        if (kb >= sb_base + 32) {
-          sb_base += 32;
-          sb_cur = sb_nxt;
-          sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
-        }
-        const float sb_kb = __shfl_sync(0xffffffffu, sb_cur, kb - sb_base);
-        const float scale = sa_kb * sb_kb;
-        const float2 scale2 = make_float2(scale, scale);
+      if constexpr (EPI) {
+        // the tile's accumulator, read once
+        const uint32_t b = np % NB, tph = (np / NB) & 1u;
+        ++np;
         if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
-        if (stage_releaser) mbar_arrive(empty(it % S));
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
         if (live) {
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
 #pragma unroll
           for (int c = 0; c < C::kEpiCols / 64; ++c) {
             float v[64];
             tmem_ld64_sync(taddr + c * 64, v);
-            if (c == C::kEpiCols / 64 - 1) {  // all of this warp's columns are in registers:
-              tc_fence_before();               // release the TMEM buffer before the last FMAs
-              __syncwarp();
-              release_tmem(b);
-            }
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = make_float2(v[2 * i], v[2 * i + 1]);
           }
-        } else {
-          tc_fence_before();
-          __syncwarp();
-          release_tmem(b);
+        }
+        tc_fence_before();
+        __syncwarp();
+        release_tmem(b);
+      } else {
+        const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
+        // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
+        // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
+        int32_t sb_base = pc.kb0 & ~31;
+        float sb_cur = (has_cols && sb_base + lane < a.KB) ? ld_nc_f32(sbp + sb_base + lane) : 0.0f;
+        float sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
+        // A-row scale of this thread's row, read from global memory kSAAhead K-block steps
+        // before use (coalesced: a warp reads 32 consecutive rows of one K block)
+        const float* sap = a.sA + grow;
+        float sa_q[kSAAhead];
+#pragma unroll
+        for (int i = 0; i < kSAAhead; ++i) {
+          const int32_t kbi = pc.kb0 + kpart + i * C::kKSplit;
+          sa_q[i] = (row_ok && kbi < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbi) * a.ld_sa) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+        for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += C::kKSplit) {
+          const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
+          const uint32_t b = it % NB, tph = (it / NB) & 1u;
+          const float sa_kb = sa_q[0];
+#pragma unroll
+          for (int i = 0; i + 1 < kSAAhead; ++i) sa_q[i] = sa_q[i + 1];
+          {
+            const int32_t kbn = kb + kSAAhead * C::kKSplit;
+            sa_q[kSAAhead - 1] =
+                (row_ok && kbn < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbn) * a.ld_sa) : 0.0f;
+          }
+          if (kb >= sb_base + 32) {
+            sb_base += 32;
+            sb_cur = sb_nxt;
+            sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
+          }
+          const float sb_kb = __shfl_sync(0xffffffffu, sb_cur, kb - sb_base);
+          const float scale = sa_kb * sb_kb;
+          const float2 scale2 = make_float2(scale, scale);
+          if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
+          if (stage_releaser) mbar_arrive(empty(it % S));
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
+          if (live) {
+#pragma unroll
+            for (int c = 0; c < C::kEpiCols / 64; ++c) {
+              float v[64];
+              tmem_ld64_sync(taddr + c * 64, v);
+              if (c == C::kEpiCols / 64 - 1) {  // all of this warp's columns are in registers:
+                tc_fence_before();               // release the TMEM buffer before the last FMAs
+                __syncwarp();
+                release_tmem(b);
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+            }
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            release_tmem(b);
+          }
         }
       }
       it_base += static_cast<uint32_t>(pc.kb1 - pc.kb0);
@@ -841,6 +909,25 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       // ---- epilogue: this warp holds rows q*32 .. q*32+31, columns ncol0 .. ncol0+kEpiCols-1
       const int nvalid = min(32, ti.rows - q * 32);
       if (nvalid <= 0 || !has_cols) continue;
+      if constexpr (EPI) {
+        // D = bf16(acc * fp32(sa[m] * sb[n])); sb is read with warp-uniform addresses (broadcast)
+        const float sa_r = row_ok ? ld_nc_f32(a.sA + (a.sa_step ? grow : 0)) : 0.0f;
+        if (a.sb_step) {
+          const float* sbp = a.sB + static_cast<int64_t>(ti.g) * a.N + ncol0;
+#pragma unroll
+          for (int j = 0; j < C::kEpiCols / 4; ++j) {
+            if (ncol0 + 4 * j < a.N) {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(sbp) + j);
+              acc[2 * j] = __fmul2_rn(acc[2 * j], make_float2(__fmul_rn(sa_r, v.x), __fmul_rn(sa_r, v.y)));
+              acc[2 * j + 1] = __fmul2_rn(acc[2 * j + 1], make_float2(__fmul_rn(sa_r, v.z), __fmul_rn(sa_r, v.w)));
+            }
+          }
+        } else {
+          const float sc = __fmul_rn(sa_r, ld_nc_f32(a.sB + ti.g));
+#pragma unroll
+          for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(sc, sc));
+        }
+      }
       if (MODE != kMasked || nvalid == 32) {
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 32; ++j) {
@@ -909,12 +996,12 @@ static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 
-template <int BN, int MODE, bool PAIR = false>
+template <int BN, int MODE, bool PAIR = false, bool EPI = false>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
                   const CUtensorMap& tD, int grid, int table_entries,
                   cudaStream_t stream) {
   using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
-  auto kern = fp8_gemm_kernel<BN, MODE, PAIR>;
+  auto kern = fp8_gemm_kernel<BN, MODE, PAIR, EPI>;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1070,11 +1157,13 @@ int env_block_n() {
 
 // Pick BN: fewest (waves x per-tile cost), the per-tile cost growing with BN plus a fixed
 // promotion/epilogue overhead.  Small-M shapes get narrow tiles so that every SM streams B.
-int choose_block_n(int64_t m_blocks, int64_t N, int sms) {
-  if (int v = env_block_n()) return v;
+// The epilogue-scaled variant has no 64-wide tiles (min_bn 128).
+int choose_block_n(int64_t m_blocks, int64_t N, int sms, int min_bn = 64) {
+  if (int v = env_block_n()) return v < min_bn ? min_bn : v;
   int best = 256;
   double best_cost = 1e300;
   for (int bn : {256, 128, 64}) {
+    if (bn < min_bn) continue;
     const int64_t tiles = m_blocks * ((N + bn - 1) / bn);
     const int64_t waves = (tiles + sms - 1) / sms;
     const double cost = static_cast<double>(waves) * (bn + 64);
@@ -1098,9 +1187,11 @@ struct Operands {
   int64_t ldd;
   int64_t rows, N, K, E, cap;
   const int32_t* groups;
+  int32_t sa_step = 0, sb_step = 0;  // epilogue-scaled variant only
 };
 
-template <int MODE>
+// EPI: the epilogue-scaled variant (per-tensor / per-token / per-channel scales)
+template <int MODE, bool EPI = false>
 int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
@@ -1108,12 +1199,12 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   if (o.rows == 0) return FP8G_OK;
 
   const int64_t m_blocks = (MODE == kMasked) ? o.E * ((o.cap + BM - 1) / BM) : (o.rows + BM - 1) / BM;
-  int bn = choose_block_n(m_blocks, o.N, dev->sm_count);
+  int bn = choose_block_n(m_blocks, o.N, dev->sm_count, EPI ? 128 : 64);
   // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
   const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
-  // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2)
-  const int pmode = env_pair();
+  // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2); the epilogue-scaled variant has single-CTA tiles
+  const int pmode = EPI ? 0 : env_pair();
   const bool pair = bn == 256 && pmode != 0 &&
                     (MODE != kDense || (o.rows + BM - 1) / BM >= 2) && dev->sm_count >= 2;
   if (pair && pmode == 2) bn = 128;
@@ -1136,6 +1227,8 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   a.groups = o.groups;
   a.status = dev->status;
   a.budget = wait_budget_cycles();
+  a.sa_step = o.sa_step;
+  a.sb_step = o.sb_step;
 
   // K blocks per stage of the variant launched below (its Cfg::kKPS)
   const uint32_t kps = small_m ? Cfg<64, true>::kKPS : 1u;
@@ -1220,6 +1313,14 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
 
   t_last_bn = bn;
   t_last_grid = grid;
+  if constexpr (EPI) {
+    if (bn == 256) {
+      t_last_stages = Cfg<256>::kStages;
+      return launch_kernel<256, MODE, false, true>(a, tA, tB, tD, grid, table_entries, stream);
+    }
+    t_last_stages = Cfg<128>::kStages;
+    return launch_kernel<128, MODE, false, true>(a, tA, tB, tD, grid, table_entries, stream);
+  }
   switch (bn) {
     case 256:
       if (pair) {
@@ -1326,6 +1427,74 @@ extern "C" int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t l
     return FP8G_ERR_ALIGNMENT;
   Operands o{A, K, sA, ld_sa, B, K, sB, D, N, static_cast<int64_t>(E) * cap, N, K, E, cap, masked_m};
   return run_gemm<kMasked>(o, static_cast<cudaStream_t>(stream));
+}
+
+// Epilogue-scaled forms: the scale arguments are checked here, the rest as in the block-scaled
+// entry points.  sA: 4-byte aligned; sB: 16-byte aligned when it has one scale per column
+// (read as float4), else 4-byte aligned.
+namespace {
+int check_epi_scales(const float* sA, int32_t sa_per_row, const float* sB, int32_t sb_per_col) {
+  if ((sa_per_row != 0 && sa_per_row != 1) || (sb_per_col != 0 && sb_per_col != 1)) return FP8G_ERR_INVALID_ARG;
+  if (!sA || !sB) return FP8G_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(sA) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sB) & (sb_per_col ? 15u : 3u)))
+    return FP8G_ERR_ALIGNMENT;
+  return FP8G_OK;
+}
+}  // namespace
+
+extern "C" int fp8_gemm_nt_scaled(const void* A, int64_t lda, const float* sA, int32_t sa_per_row,
+                                  const void* B, int64_t ldb, const float* sB, int32_t sb_per_col,
+                                  void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
+  if (M < 0 || M > kMaxI32 || N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 ||
+      K > kMaxI32 || lda < K || ldb < K || ldd < N)
+    return FP8G_ERR_INVALID_ARG;
+  if (sa_per_row != 0 && sa_per_row != 1) return FP8G_ERR_INVALID_ARG;
+  if (sb_per_col != 0 && sb_per_col != 1) return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;
+  if (!A || !B || !D) return FP8G_ERR_INVALID_ARG;
+  if (int st = check_epi_scales(sA, sa_per_row, sB, sb_per_col)) return st;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, lda, sA, 0, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr, sa_per_row, sb_per_col};
+  return run_gemm<kDense, true>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_contiguous_scaled(const void* A, const float* sA, int32_t sa_per_row,
+                                                  const void* B, const float* sB, int32_t sb_per_col,
+                                                  void* D, const int32_t* group_offsets, int32_t E,
+                                                  int64_t M_total, int64_t N, int64_t K, void* stream) {
+  if (E < 1 || E > kMaxExperts || M_total < 0 || M_total > kMaxI32 || M_total % 128 != 0 ||
+      N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32)
+    return FP8G_ERR_INVALID_ARG;
+  if (sa_per_row != 0 && sa_per_row != 1) return FP8G_ERR_INVALID_ARG;
+  if (sb_per_col != 0 && sb_per_col != 1) return FP8G_ERR_INVALID_ARG;
+  if (M_total == 0) return FP8G_OK;
+  if (!A || !B || !D || !group_offsets) return FP8G_ERR_INVALID_ARG;
+  if (int st = check_epi_scales(sA, sa_per_row, sB, sb_per_col)) return st;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, K, sA, 0, B, K, sB, D, N, M_total, N, K, E, 0, group_offsets, sa_per_row, sb_per_col};
+  return run_gemm<kContiguous, true>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_masked_scaled(const void* A, const float* sA, int32_t sa_per_row,
+                                              const void* B, const float* sB, int32_t sb_per_col,
+                                              void* D, const int32_t* masked_m, int32_t E, int64_t cap,
+                                              int64_t N, int64_t K, void* stream) {
+  if (E < 1 || E > kMaxExperts || cap < 0 || cap % 16 != 0 || static_cast<int64_t>(E) * cap > kMaxI32 ||
+      N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32)
+    return FP8G_ERR_INVALID_ARG;
+  if (sa_per_row != 0 && sa_per_row != 1) return FP8G_ERR_INVALID_ARG;
+  if (sb_per_col != 0 && sb_per_col != 1) return FP8G_ERR_INVALID_ARG;
+  if (cap == 0) return FP8G_OK;
+  if (!A || !B || !D || !masked_m) return FP8G_ERR_INVALID_ARG;
+  if (int st = check_epi_scales(sA, sa_per_row, sB, sb_per_col)) return st;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (reinterpret_cast<uintptr_t>(masked_m) & 3u))
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, K, sA, 0, B, K, sB, D, N, static_cast<int64_t>(E) * cap, N, K, E, cap, masked_m,
+             sa_per_row, sb_per_col};
+  return run_gemm<kMasked, true>(o, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8g_last_config(int* block_n, int* stages, int* grid) {

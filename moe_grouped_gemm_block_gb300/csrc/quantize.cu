@@ -11,6 +11,7 @@
 // could round differently) and the round-to-nearest-even saturating e4m3 conversion.
 
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -237,6 +238,116 @@ __global__ void __launch_bounds__(256) quantize_128x128_kernel(
 // follow the entries' order, i.e. ascending tokens.  Ids outside [0, E) are dropped and flag
 // FP8G_ERR_DEVICE_ASSERT; if the padded rows would not fit into M_cap, the layout is left empty
 // (all offsets 0) and the same status is raised.
+// ---- per-token / per-channel (one scale per row over the whole K) and per-tensor scales
+// ("DeepGEMM FP8 walk-through" sec. 2.2); same scale and code rules as the block forms.
+
+// One CTA per row.  The row's 16-byte pieces are held in registers (rows of up to
+// kRowThreads * kRowVec * 8 values) between the amax reduction and the quantisation; longer
+// rows read the rest again (from L1 / L2).
+constexpr int kRowThreads = 256;
+constexpr int kRowVec = 8;
+
+__device__ __forceinline__ float block_amax(float a, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = a;
+  __syncthreads();
+  float m = 0.0f;
+  for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+__global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
+    float* __restrict__ s_out) {
+  __shared__ float red[kRowThreads / 32];
+  const int64_t m = blockIdx.x;
+  const int t = threadIdx.x;
+  const int64_t nvec = K / 8;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + m * ldx);
+  uint2* qr = reinterpret_cast<uint2*>(q + m * ldq);
+  uint4 raw[kRowVec];
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int64_t v = t + static_cast<int64_t>(i) * kRowThreads;
+    raw[i] = v < nvec ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    float f[8];
+    unpack8(raw[i], f);
+    a = fmaxf(a, amax8(f));
+  }
+  for (int64_t v = t + kRowVec * kRowThreads; v < nvec; v += kRowThreads) {
+    float f[8];
+    unpack8(__ldg(xr + v), f);
+    a = fmaxf(a, amax8(f));
+  }
+  const float amax = block_amax(a, red);
+  const float s = __fdiv_rn(amax, kE4M3Max);
+  const bool direct = direct_ok(amax, s);
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int64_t v = t + static_cast<int64_t>(i) * kRowThreads;
+    if (v < nvec) {
+      float f[8];
+      unpack8(raw[i], f);
+      qr[v] = quant8(f, s, direct);
+    }
+  }
+  for (int64_t v = t + kRowVec * kRowThreads; v < nvec; v += kRowThreads) {
+    float f[8];
+    unpack8(__ldg(xr + v), f);
+    qr[v] = quant8(f, s, direct);
+  }
+  if (t == 0) s_out[m] = s;
+}
+
+// Per-tensor, pass 1: tensor e = blockIdx.y (rows e*M .. e*M+M-1).  Each CTA raises s[e] to
+// RN(amax_cta / 448) with an integer max on the bits: for non-negative floats the bit order is
+// the value order, and RN(a / 448) is non-decreasing in a, so the largest of the CTAs' values is
+// RN(amax / 448) of the whole tensor.  s[e] starts at +0.
+constexpr int kTensorThreads = 256;
+
+__global__ void __launch_bounds__(kTensorThreads) tensor_scale_kernel(
+    const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t kvec, int64_t ldx, float* __restrict__ s) {
+  __shared__ float red[kTensorThreads / 32];
+  const uint32_t e = blockIdx.y;
+  const uint32_t total = M * kvec;  // the host guarantees M * K / 8 < 2^31
+  float a = 0.0f;
+  for (uint32_t p = blockIdx.x * kTensorThreads + threadIdx.x; p < total; p += gridDim.x * kTensorThreads) {
+    const uint32_t r = p / kvec, v = p - r * kvec;
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x + (static_cast<int64_t>(e) * M + r) * ldx) + v), f);
+    a = fmaxf(a, amax8(f));
+  }
+  const float amax = block_amax(a, red);
+  if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(s) + e, __float_as_uint(__fdiv_rn(amax, kE4M3Max)));
+}
+
+// Per-tensor, pass 2: the codes with the tensor's scale.  The direct-product test needs amax's
+// bf16 significand, recovered from s: for s normal, s * 448 is within 2^-23 (relative) of amax,
+// far inside half a bf16 step, so rounding it to bf16 gives amax back.  (For s subnormal or zero
+// the test is not used.)
+__global__ void __launch_bounds__(kTensorThreads) quantize_tensor_kernel(
+    const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t kvec, int64_t ldx, uint8_t* __restrict__ q,
+    int64_t ldq, const float* __restrict__ s_in) {
+  const uint32_t e = blockIdx.y;
+  const float s = __ldg(s_in + e);
+  const float amax = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s, kE4M3Max)));
+  const bool direct = direct_ok(amax, s);
+  const uint32_t total = M * kvec;
+  for (uint32_t p = blockIdx.x * kTensorThreads + threadIdx.x; p < total; p += gridDim.x * kTensorThreads) {
+    const uint32_t r = p / kvec, v = p - r * kvec;
+    const int64_t row = static_cast<int64_t>(e) * M + r;
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x + row * ldx) + v), f);
+    reinterpret_cast<uint2*>(q + row * ldq)[v] = quant8(f, s, direct);
+  }
+}
+
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteMaxExperts = 2048;
 constexpr int kRouteChunk = 4096;  // entries staged in shared memory per pass of the assigning warp
@@ -471,6 +582,57 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
   quantize_1x128_kernel<true><<<static_cast<unsigned>(blocks), kQThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M_cap), static_cast<uint32_t>(K / 128), ldx,
       static_cast<uint8_t*>(q), ldq, sA, ld_sa, row_token);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+extern "C" int fp8_quantize_per_row(const void* x, int64_t M, int64_t K, int64_t ldx, void* q,
+                                    int64_t ldq, float* s, void* stream) {
+  if (M < 0 || M > 0x7FFFFFFF || K <= 0 || K % 128 != 0 || ldx < K || ldq < K) return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;
+  if (!x || !q || !s) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s) & 3u) || ldx % 8 != 0 || ldq % 16 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  quantize_rows_kernel<<<static_cast<unsigned>(M), kRowThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), K, ldx, static_cast<uint8_t*>(q), ldq, s);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+extern "C" int fp8_quantize_per_tensor(const void* x, int64_t E, int64_t M, int64_t K, int64_t ldx, void* q,
+                                       int64_t ldq, float* s, void* stream) {
+  if (E < 1 || E > 65535 || M < 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq < K) return FP8G_ERR_INVALID_ARG;
+  if (M * (K / 8) >= (int64_t{1} << 31)) return FP8G_ERR_INVALID_ARG;
+  if (!s) return FP8G_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(s) & 3u)) return FP8G_ERR_ALIGNMENT;
+  if (M > 0) {
+    if (!x || !q) return FP8G_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || ldx % 8 != 0 || ldq % 16 != 0) return FP8G_ERR_ALIGNMENT;
+  }
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // s starts at +0, the scale of an empty or all-zero tensor
+  if (cudaMemsetAsync(s, 0, static_cast<size_t>(E) * 4, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8G_ERR_CUDA;
+  }
+  if (M == 0) return FP8G_OK;
+  const uint32_t kvec = static_cast<uint32_t>(K / 8);
+  const int64_t pieces = M * (K / 8);
+  int64_t bx = (pieces + kTensorThreads - 1) / kTensorThreads;
+  // enough CTAs per tensor to fill the GPU across all E tensors
+  const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(dev->sm_count) * (2048 / kTensorThreads) / E);
+  if (bx > cap) bx = cap;
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(E));
+  tensor_scale_kernel<<<grid, kTensorThreads, 0, cs>>>(static_cast<const __nv_bfloat16*>(x),
+                                                       static_cast<uint32_t>(M), kvec, ldx, s);
+  if (cudaGetLastError() != cudaSuccess) return FP8G_ERR_CUDA;
+  quantize_tensor_kernel<<<grid, kTensorThreads, 0, cs>>>(static_cast<const __nv_bfloat16*>(x),
+                                                          static_cast<uint32_t>(M), kvec, ldx,
+                                                          static_cast<uint8_t*>(q), ldq, s);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

@@ -121,3 +121,53 @@ def test_gemm_nt_noalloc_validation(lib, kw, want):
 
 def test_gemm_nt_noalloc_m_zero_is_a_noop(lib):
     assert lib.fp8_gemm_nt_noalloc(*_nt(M=0, A=None, sA=None, B=None, sB=None, D=None)) == 0
+
+
+def _nts(**kw):
+    a = dict(A=P, lda=256, sA=P, pa=1, B=P, ldb=256, sB=P, pb=1, D=P, ldd=256, M=64, N=256, K=256, s=None)
+    a.update(kw)
+    return tuple(a.values())
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(K=200), INVALID), (dict(N=250), INVALID), (dict(M=-1), INVALID), (dict(ldd=128), INVALID),
+    (dict(pa=2), INVALID), (dict(pb=-1), INVALID), (dict(A=None), INVALID), (dict(sA=None), INVALID),
+    (dict(A=P + 1), ALIGN), (dict(lda=264), ALIGN), (dict(sA=P + 2), ALIGN),
+    (dict(sB=P + 4), ALIGN),            # one scale per column: float4 reads need 16-byte alignment
+])
+def test_gemm_nt_scaled_validation(lib, kw, want):
+    assert lib.fp8_gemm_nt_scaled(*_nts(**kw)) == want
+
+
+def test_gemm_nt_scaled_per_tensor_b_needs_only_4_byte_alignment(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present: covered by the GPU tests")
+    # passes validation (then fails for want of a device)
+    assert lib.fp8_gemm_nt_scaled(*_nts(sB=P + 4, pb=0)) in (3, 4)
+    assert lib.fp8_gemm_nt_scaled(*_nts(M=0, A=None, sA=None, B=None, sB=None, D=None)) == 0
+
+
+def test_grouped_scaled_validation(lib):
+    c, m = lib.fp8_grouped_gemm_contiguous_scaled, lib.fp8_grouped_gemm_masked_scaled
+    assert c(P, P, 1, P, P, 1, P, P, 0, 256, 256, 256, None) == INVALID      # E
+    assert c(P, P, 1, P, P, 1, P, P, 2, 200, 256, 256, None) == INVALID      # M_total % 128
+    assert c(P, P, 3, P, P, 1, P, P, 2, 256, 256, 256, None) == INVALID      # mode flag
+    assert c(P, P, 1, P, P, 1, P, None, 2, 256, 256, 256, None) == INVALID   # offsets
+    assert c(P, P, 1, P, P + 8, 1, P, P, 2, 256, 256, 256, None) == ALIGN
+    assert m(P, P, 1, P, P, 1, P, P, 2, 100, 256, 256, None) == INVALID      # cap % 16
+    assert m(P, P, 1, P, P, 0, P, P, 2, 128, 250, 256, None) == INVALID      # N % 16
+    assert m(P, P + 1, 1, P, P, 0, P, P, 2, 128, 256, 256, None) == ALIGN
+
+
+def test_quantise_per_row_and_per_tensor_validation(lib):
+    r, t = lib.fp8_quantize_per_row, lib.fp8_quantize_per_tensor
+    assert r(P, 4, 100, 128, P, 128, P, None) == INVALID      # K % 128
+    assert r(P, 4, 128, 64, P, 128, P, None) == INVALID       # ldx < K
+    assert r(P, 0, 128, 128, None, 128, None, None) == 0      # M == 0: no-op
+    assert r(P + 8, 4, 128, 128, P, 128, P, None) == ALIGN
+    assert r(P, 4, 128, 128, P, 136, P, None) == ALIGN        # ldq % 16
+    assert t(P, 0, 4, 128, 128, P, 128, P, None) == INVALID   # E
+    assert t(P, 1, 4, 128, 128, P, 128, None, None) == INVALID
+    assert t(P, 1, 4, 128, 128, P, 128, P + 2, None) == ALIGN
+    assert t(P, 1, 1 << 28, 128, 128, P, 128, P, None) == INVALID  # M * K / 8 >= 2^31
