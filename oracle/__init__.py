@@ -18,6 +18,9 @@ Modules:
   route     -- the contiguous grouped layout built from routed tokens, gathered and quantised
   scaled    -- per-tensor / per-token / per-channel quantisation and the GEMM that applies
                those scales once, in the epilogue, with its grouped forms
+  e5m2      -- the e5m2 (OCP "E5M2") codec for gradients
+  backward  -- 1x128 e5m2 gradient quantisation, the data-gradient GEMM (e5m2 x e4m3) and the
+               K-grouped weight-gradient GEMM of a grouped MoE layer
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 invariants, brute force on tiny inputs and library routines; none is "parity
 unpinned".
@@ -27,6 +30,8 @@ from .e4m3 import E4M3_MAX, e4m3_decode, e4m3_decode_table, e4m3_encode, bf16_ro
 from .quantize import quantize_1x128, quantize_128x128
 from .gemm import gemm_nt, grouped_contiguous, grouped_masked
 from .route import route_gather_quantize, route_layout
+from .backward import block_products, gemm_nt_dgrad, quantize_1x128_e5m2, wgrad_k_grouped
+from .e5m2 import E5M2_MAX, e5m2_decode, e5m2_encode
 from .scaled import (gemm_nt_scaled, grouped_contiguous_scaled, grouped_masked_scaled, quantize_per_row,
                      quantize_per_tensor)
 
@@ -35,4 +40,6 @@ __all__ = [
     "bf16_bits_to_f32", "quantize_1x128", "quantize_128x128", "gemm_nt", "grouped_contiguous",
     "grouped_masked", "route_gather_quantize", "route_layout", "gemm_nt_scaled",
     "grouped_contiguous_scaled", "grouped_masked_scaled", "quantize_per_row", "quantize_per_tensor",
+    "E5M2_MAX", "e5m2_decode", "e5m2_encode", "block_products", "gemm_nt_dgrad", "quantize_1x128_e5m2",
+    "wgrad_k_grouped",
 ]
