@@ -468,6 +468,51 @@ def measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak, reps=20):
         "workload": f"moe_contiguous, per-token A x per-channel B: M_total={A.shape[0]}, E={E}, N={N}, K={K}",
         "us": round(us, 2), "tflops": round(tf, 1), "pct_fp8_peak": round(100 * tf / fp8_peak, 1), "launches": 1}
     del qa, qb, D
+    out.update(measure_backward_rows(g, dev, flush, hbm_peak, fp8_peak, inp, w, reps))
+    return out
+
+
+def measure_backward_rows(g, dev, flush, hbm_peak, fp8_peak, inp, w, reps):
+    """The backward pass of the MoE contiguous layer with e5m2 gradients: a seeded synthetic output
+    gradient dY ~ N(0, 1e-3) [M_total, N] (zero on padding rows), quantised 1x128 to e5m2; the grouped
+    data gradient dX = dY W_e (B = each expert's W^T, 128x128 blocks); the K-grouped weight gradient
+    dW[e] = dY_e^T X_e over each expert's tokens (both operands transposed and quantised 1x128 along
+    tokens, untimed setup)."""
+    A, B = inp["A"], inp["B"]
+    E, N, K = B.shape
+    M_total = A.shape[0]
+    offs = inp["group_offsets"].to(dev)
+    valid = (inp["row_token"] >= 0).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(77)
+    dY = (torch.randn((M_total, N), generator=gen, device=dev) * 1e-3 * valid[:, None]).to(torch.bfloat16)
+    flops = 2.0 * w.tokens * w.topk * N * K
+    out = {}
+    qdy, sdy = g.quantize_1x128_e5m2(dY)
+    us = _time_calls(lambda: g.fp8_quantize_1x128_e5m2(dY, qdy, sdy), flush, reps)
+    qbytes = M_total * N * 3 + M_total * (N // 128) * 4
+    out["quantize_1x128_e5m2"] = {"workload": f"dY of moe_contiguous: {M_total} x {N} bf16", "us": round(us, 2),
+                                  "gbs": round(qbytes / (us * 1e-6) / 1e9, 1),
+                                  "pct_hbm_peak": round(100 * qbytes / (us * 1e-6) / 1e9 / hbm_peak, 1),
+                                  "launches": 1}
+    qwt, swt = g.quantize_128x128(B.transpose(1, 2).contiguous())  # [E, K, N]
+    dX = torch.empty((M_total, K), dtype=torch.bfloat16, device=dev)
+    us = _time_calls(lambda: g.fp8_grouped_gemm_contiguous_dgrad(qdy, sdy, qwt, swt, dX, offs), flush, reps)
+    tf = flops / (us * 1e-6) / 1e12
+    out["grouped_gemm_contiguous_dgrad"] = {
+        "workload": f"moe_contiguous backward, dX = dY W: M_total={M_total}, E={E}, N={K}, K={N}",
+        "us": round(us, 2), "tflops": round(tf, 1), "pct_fp8_peak": round(100 * tf / fp8_peak, 1), "launches": 1}
+    del qwt, dX
+    qdyT, sdyT = g.quantize_1x128_e5m2(dY.t().contiguous())   # [N, M_total]
+    qxT, sxT = g.quantize_1x128(A.t().contiguous())           # [K, M_total]
+    dW = torch.empty((E, N, K), dtype=torch.bfloat16, device=dev)
+    us = _time_calls(lambda: g.fp8_grouped_gemm_wgrad(qdyT, sdyT, qxT, sxT, dW, offs), flush, reps)
+    tf = flops / (us * 1e-6) / 1e12
+    out["grouped_gemm_wgrad"] = {
+        "workload": f"moe_contiguous backward, dW[e] = dY_e^T X_e over each expert's tokens: E={E}, M={N}, N={K}, "
+                    f"T={M_total}", "us": round(us, 2), "tflops": round(tf, 1),
+        "pct_fp8_peak": round(100 * tf / fp8_peak, 1), "launches": 1, "config": g.fp8g_last_config()}
+    if g.fp8g_get_status() != 0:
+        raise RuntimeError("device status not OK after the backward rows")
     return out
 
 

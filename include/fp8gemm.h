@@ -295,6 +295,60 @@ int fp8_grouped_gemm_masked_scaled(const void* A, const float* sA, int32_t sa_pe
                                    int64_t K, void* stream);
 
 /*
+ * Backward GEMMs with e5m2 gradients ("DeepGEMM FP8 walk-through" sec. 2.1 and "Production FP8
+ * GEMM alignment and Tensor Core peak tuning", "E4M3 vs E5M2": gradients use e5m2, 1-5-2 bits,
+ * range to 57344; OCP "E5M2", with infinities and NaN in the top exponent).
+ */
+
+/*
+ * fp8_quantize_1x128_e5m2 -- fp8_quantize_1x128 for gradients: s = fp32(amax / 57344), codes
+ * e5m2 (round-to-nearest-even, saturating to +-57344).  Same arguments, layout and errors.
+ */
+int fp8_quantize_1x128_e5m2(const void* x, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                            float* sA, int64_t ld_sa, void* stream);
+
+/*
+ * fp8_gemm_nt_dgrad -- the data gradient dX = dY * W as fp8_gemm_nt: A = dY holds e5m2 codes
+ * (1x128 scales from fp8_quantize_1x128_e5m2), B = W^T [K_in, N] holds e4m3 codes with 128x128
+ * block scales.  Arguments, layout and errors as fp8_gemm_nt.
+ */
+int fp8_gemm_nt_dgrad(const void* A, int64_t lda, const float* sA, int64_t ld_sa, const void* B,
+                      int64_t ldb, const float* sB, void* D, int64_t ldd, int64_t M, int64_t N,
+                      int64_t K, void* stream);
+
+/*
+ * fp8_grouped_gemm_contiguous_dgrad -- the data gradient of a grouped MoE layer: as
+ * fp8_grouped_gemm_contiguous with A = dY in e5m2 (1x128 scales) and B [E, K_in, N] = each
+ * expert's W^T in e4m3 (128x128 block scales).  Arguments, layout and errors as
+ * fp8_grouped_gemm_contiguous.
+ */
+int fp8_grouped_gemm_contiguous_dgrad(const void* A, const float* sA, int64_t ld_sa, const void* B,
+                                      const float* sB, void* D, const int32_t* group_offsets,
+                                      int32_t E, int64_t M_total, int64_t N, int64_t K, void* stream);
+
+/*
+ * fp8_grouped_gemm_wgrad -- the weight gradient of a grouped MoE layer, one matrix per expert,
+ * contracting over that expert's tokens ("K-grouped"):
+ *     D[e] = sum over tokens t of expert e of  A[:, t] (x) B[:, t]      (dW[e] = dY_e^T * X_e)
+ * with the block promotion acc += P_kb * (sA[kb][m] * sB[kb][n]) over the expert's 128-token
+ * blocks, FP32 accumulation, BF16 output.  An expert with no tokens gets D[e] = 0.
+ *
+ *   A        e5m2 [M, T] (dY^T: output channels x tokens), row stride lda bytes (lda >= T, % 16)
+ *   sA       fp32 [T/128][ld_sa] (ld_sa >= M, % 4), as fp8_quantize_1x128_e5m2 writes it for A
+ *   B        e4m3 [N, T] (X^T: input channels x tokens), row stride ldb bytes (ldb >= T, % 16)
+ *   sB       fp32 [T/128][ld_sb] (ld_sb >= N, % 4), as fp8_quantize_1x128 writes it for B
+ *   D        bf16 [E, M, N], contiguous
+ *   offsets  int32 [E+1], DEVICE memory: expert e owns tokens offsets[e] .. offsets[e+1]-1;
+ *            non-decreasing multiples of 128, offsets[E] <= T (tokens past it belong to no
+ *            expert).  Violations make the kernel write nothing and set FP8G_ERR_DEVICE_ASSERT.
+ *   1 <= E <= 2048, M >= 0 and M % 16 == 0 (M == 0: no-op), E*M < 2^31, N % 16 == 0,
+ *   T % 128 == 0.  Pointers 16-byte aligned.
+ */
+int fp8_grouped_gemm_wgrad(const void* A, int64_t lda, const float* sA, int64_t ld_sa, const void* B,
+                           int64_t ldb, const float* sB, int64_t ld_sb, void* D, const int32_t* offsets,
+                           int32_t E, int64_t M, int64_t N, int64_t T, void* stream);
+
+/*
  * fp8g_get_status -- synchronise `stream`, then return and clear the current
  * device's status word (FP8G_OK if no kernel recorded an error since the last
  * call).  Returns FP8G_ERR_CUDA if the synchronisation itself fails.

@@ -14,6 +14,10 @@ functions here carry the same names and take torch tensors:
     fp8_gemm_nt_scaled(A, sA, B, sB, D)                  epilogue scales: sA [M] or [1], sB [N] or [1]
     fp8_grouped_gemm_contiguous_scaled(A, sA, B, sB, D, group_offsets)   sB [E,N] or [E]
     fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m)
+    fp8_quantize_1x128_e5m2(x, q, sA)                  gradients: e5m2 codes, s = amax / 57344
+    fp8_gemm_nt_dgrad(A, sA, B, sB, D)                 data gradient: A e5m2 [M,K], B e4m3 [N,K] (= W^T)
+    fp8_grouped_gemm_contiguous_dgrad(A, sA, B, sB, D, group_offsets)   grouped data gradient
+    fp8_grouped_gemm_wgrad(A, sA, B, sB, D, offsets)   weight gradient per expert over its tokens
 
 e4m3 tensors may be torch.uint8 or torch.float8_e4m3fn.  Work is enqueued on the
 current CUDA stream of the tensors' device.  A non-zero status raises Fp8GemmError.
@@ -63,6 +67,10 @@ _SIGNATURES = {
     "fp8_gemm_nt_scaled": [_P, _I64, _FP, _I32, _P, _I64, _FP, _I32, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_contiguous_scaled": [_P, _FP, _I32, _P, _FP, _I32, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_masked_scaled": [_P, _FP, _I32, _P, _FP, _I32, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8_quantize_1x128_e5m2": [_P, _I64, _I64, _I64, _P, _I64, _FP, _I64, _P],
+    "fp8_gemm_nt_dgrad": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_contiguous_dgrad": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_wgrad": [_P, _I64, _FP, _I64, _P, _I64, _FP, _I64, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8g_get_status": [_P],
     "fp8g_last_config": [ctypes.POINTER(ctypes.c_int)] * 3,
 }
@@ -261,6 +269,63 @@ def fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m) -> None:
            "fp8_grouped_gemm_masked_scaled")
 
 
+def fp8_quantize_1x128_e5m2(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor) -> None:
+    _need(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1, "x: bf16 [M,K], K contiguous")
+    _need(q.dtype in (torch.uint8, torch.float8_e5m2) and q.shape == x.shape and q.stride(1) == 1, "q: e5m2 [M,K]")
+    M, K = x.shape
+    _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1,
+          "sA: f32 [K/128, ld_sa]")
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_quantize_1x128_e5m2(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(sA), ld_sa,
+                                         _stream(x)), "fp8_quantize_1x128_e5m2")
+
+
+def fp8_gemm_nt_dgrad(A, sA, B, sB, D) -> None:
+    """fp8_gemm_nt with A in e5m2 (the output gradient dY) and B = W^T in e4m3."""
+    _need(A.dtype in (torch.uint8, torch.float8_e5m2) and A.dim() == 2 and A.stride(1) == 1, "A: e5m2 [M,K]")
+    _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
+    _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
+    _need(sA.dtype == torch.float32 and sB.dtype == torch.float32 and sB.is_contiguous(), "scales: f32")
+    M, K = A.shape
+    N = B.shape[0]
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_gemm_nt_dgrad(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
+                                   _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt_dgrad")
+
+
+def fp8_grouped_gemm_contiguous_dgrad(A, sA, B, sB, D, group_offsets) -> None:
+    """fp8_grouped_gemm_contiguous with A in e5m2 (dY) and B [E, K_in, N] = each expert's W^T."""
+    _need(A.dtype in (torch.uint8, torch.float8_e5m2) and A.dim() == 2 and A.is_contiguous(),
+          "A: e5m2 [M_total,K] contiguous")
+    _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
+    _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [M_total,N] contiguous")
+    _need(group_offsets.dtype == torch.int32 and group_offsets.is_cuda, "group_offsets: int32 device tensor")
+    M_total, K = A.shape
+    E, N, _ = B.shape
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_grouped_gemm_contiguous_dgrad(_ptr(A), _ptr(sA), ld_sa, _ptr(B), _ptr(sB), _ptr(D),
+                                                   _ptr(group_offsets), E, M_total, N, K, _stream(A)),
+           "fp8_grouped_gemm_contiguous_dgrad")
+
+
+def fp8_grouped_gemm_wgrad(A, sA, B, sB, D, offsets) -> None:
+    """A e5m2 [M,T] (dY^T), sA f32 [T/128, ld_sa]; B e4m3 [N,T] (X^T), sB f32 [T/128, ld_sb];
+    D bf16 [E,M,N]; offsets int32 [E+1] device (token ranges per expert, multiples of 128)."""
+    _need(A.dtype in (torch.uint8, torch.float8_e5m2) and A.dim() == 2 and A.stride(1) == 1, "A: e5m2 [M,T]")
+    _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,T]")
+    _need(D.dtype == torch.bfloat16 and D.dim() == 3 and D.is_contiguous(), "D: bf16 [E,M,N] contiguous")
+    _need(offsets.dtype == torch.int32 and offsets.is_cuda, "offsets: int32 device tensor")
+    M, T = A.shape
+    N = B.shape[0]
+    E = D.shape[0]
+    _need(offsets.numel() == E + 1 and D.shape[1:] == (M, N), "shapes")
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    ld_sb = sB.stride(0) if sB.shape[0] > 1 else sB.shape[1]
+    _check(lib().fp8_grouped_gemm_wgrad(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
+                                        ld_sb, _ptr(D), _ptr(offsets), E, M, N, T, _stream(A)),
+           "fp8_grouped_gemm_wgrad")
+
+
 def fp8g_get_status(stream: torch.cuda.Stream | None = None) -> int:
     s = (stream or torch.cuda.current_stream()).cuda_stream
     return lib().fp8g_get_status(s)
@@ -341,6 +406,16 @@ def quantize_per_tensor(x: torch.Tensor):
     s = torch.empty(1 if x.dim() == 2 else x.shape[0], dtype=torch.float32, device=x.device)
     fp8_quantize_per_tensor(x, q, s)
     return q, s
+
+
+def quantize_1x128_e5m2(x: torch.Tensor, ld_sa: int | None = None):
+    """bf16 [M,K] gradients -> (q uint8 e5m2 [M,K], sA f32 [K/128, ld_sa])."""
+    M, K = x.shape
+    ld = ld_sa or max(round_up(M, 4), 4)
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sA = torch.zeros((K // 128, ld), dtype=torch.float32, device=x.device)
+    fp8_quantize_1x128_e5m2(x, q, sA)
+    return q, sA
 
 
 def gemm_nt_scaled(A, sA, B, sB) -> torch.Tensor:

@@ -49,7 +49,10 @@ namespace fp8g {
 namespace {
 
 // kDenseSmallM: dense with M <= 64 (decode shapes), BN = 64 only: loads 64 A rows per stage.
-enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3 };
+// kKGrouped: the weight gradient of a grouped layer -- one output matrix per expert, the
+// contraction running over that expert's token range (offsets in the group table), both
+// operands with one scale per row and 128-token block.
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3, kKGrouped = 4 };
 
 constexpr int BM = 128;  // rows per tile = TMEM lanes
 constexpr int BK = 128;  // K per stage = the scaling block
@@ -134,6 +137,10 @@ struct GemmArgs {
   // epilogue scaling: sA holds one scale per row of A (sa_step 1) or one for all rows (0); sB one
   // per column of each expert, [E][N] (sb_step 1), or one per expert, [E] (0)
   int32_t sa_step, sb_step;
+  // operand formats in the MMA instruction descriptor (A bits 7-9, B bits 10-12; 0 = e4m3, 1 = e5m2)
+  uint32_t idesc_fmt;
+  int64_t ld_sb;  // kKGrouped: B scales [K blocks][ld_sb], one per row of B
+
   // stream-K tail (see make_work): on/off, its minimum K blocks per CTA, and the workspace of
   // FP32 partial tiles (one slot per CTA) with one ready flag per CTA (zeroed before the launch)
   int32_t sk;
@@ -144,10 +151,12 @@ struct GemmArgs {
 };
 
 struct Tile {
-  int32_t a_row;  // first row of A / D (and the x coordinate into the scale map)
+  int32_t a_row;  // first row of A (and of the A scales)
   int32_t n0;     // first column
   int32_t g;      // expert
   int32_t rows;   // rows of the tile that may be stored (masked tail), else BM
+  int32_t d_row;  // first row of D (a_row, except kKGrouped: expert * M + a_row)
+  int32_t kb_first, kb_count;  // the tile's K blocks (0 and KB, except kKGrouped: its expert's tokens)
 };
 
 // The work of one CTA, as pieces (tile, K blocks kb0 .. kb1 - 1).  Whole tiles c, c + G, ...
@@ -241,6 +250,26 @@ __device__ __forceinline__ bool next_piece(Work& w, Piece& p) {
 template <int BN, int MODE>
 __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table, int32_t t,
                                          Tile& ti) {
+  ti.kb_first = 0;
+  ti.kb_count = a.KB;
+  if (MODE == kKGrouped) {
+    // expert e = t / (m-blocks x n-blocks), then the dense banded raster within the expert
+    const int32_t per_e = a.num_m * a.num_n;
+    const int32_t e = t / per_e, r = t - e * per_e;
+    const int32_t band_tiles = kBandM * a.num_n;
+    const int32_t band = r / band_tiles, rr = r - band * band_tiles;
+    const int32_t m_first = band * kBandM;
+    const int32_t gm = min(kBandM, a.num_m - m_first);
+    const int32_t mb = m_first + rr % gm, nb = rr / gm;
+    ti.g = e;
+    ti.a_row = mb * BM;
+    ti.n0 = nb * BN;
+    ti.rows = min(BM, a.rows - ti.a_row);
+    ti.d_row = e * a.rows + ti.a_row;
+    ti.kb_first = table[e] / BK;
+    ti.kb_count = (table[e + 1] - table[e]) / BK;  // 0 for an expert without tokens: zeros
+    return true;
+  }
   if (MODE == kMasked) {
     // table[e] = sum of m-blocks of experts < e; an expert's tiles are (nb, mb), mb fastest
     int lo = 0, hi = a.E;  // find e with table[e]*num_n <= t < table[e+1]*num_n
@@ -257,6 +286,7 @@ __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table
     cnt = min(max(cnt, 0), a.cap);
     ti.g = e;
     ti.a_row = e * a.cap + mb * BM;
+    ti.d_row = ti.a_row;
     ti.n0 = nb * BN;
     ti.rows = min(BM, cnt - mb * BM);
     return ti.rows > 0;
@@ -267,6 +297,7 @@ __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table
     const int32_t gm = min(kBandM, a.num_m - m_first);
     const int32_t mb = m_first + r % gm, nb = r / gm;
     ti.a_row = mb * BM;
+    ti.d_row = ti.a_row;
     ti.n0 = nb * BN;
     ti.rows = min(BM, a.rows - ti.a_row);  // rows past the matrix edge are not stored
     ti.g = 0;
@@ -291,6 +322,8 @@ __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table
 template <int BN, int MODE>
 __device__ __forceinline__ void get_pair_tile(const GemmArgs& a, const int32_t* table, const int32_t* ptab,
                                               int32_t t, uint32_t rank, Tile& ti) {
+  ti.kb_first = 0;
+  ti.kb_count = a.KB;
   if (MODE == kDense) {
     constexpr int kBand = kBandM / 2;  // pairs per raster band
     const int32_t num_mp = (a.num_m + 1) >> 1;
@@ -300,6 +333,7 @@ __device__ __forceinline__ void get_pair_tile(const GemmArgs& a, const int32_t* 
     const int32_t gm = min(kBand, num_mp - p_first);
     const int32_t mp = p_first + r % gm, nb = r / gm;
     ti.a_row = (2 * mp + static_cast<int32_t>(rank)) * BM;
+    ti.d_row = ti.a_row;
     ti.n0 = nb * BN;
     ti.rows = min(BM, a.rows - ti.a_row);
     ti.g = 0;
@@ -328,6 +362,7 @@ __device__ __forceinline__ void get_pair_tile(const GemmArgs& a, const int32_t* 
     ti.a_row = e * a.cap + mb * BM;
     ti.rows = min(BM, cnt - mb * BM);
   }
+  ti.d_row = ti.a_row;
 }
 
 // Bounded wait on an mbarrier phase.  On timeout: flag the CTA, record the status.
@@ -381,6 +416,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
   static_assert(!EPI || (C::kKSplit == 1 && C::kMmaWarps == 1 && !PAIR),
                 "epilogue scaling: one K part, one issuer, single-CTA tiles");
+  static_assert(MODE != kKGrouped || (!EPI && !PAIR && C::kMmaWarps == 1),
+                "K-grouped: block-scaled single-CTA tiles with one issuer");
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_u32(smem);
@@ -440,12 +477,14 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   // pair tiles per expert (prefix over experts), after the group table
   int32_t* ptab = table + (a.E + 1);
   // Group tables (grouped modes), built by the first epilogue warp.
-  if (MODE == kContiguous && warp == C::kEpiWarp0) {
+  if ((MODE == kContiguous || MODE == kKGrouped) && warp == C::kEpiWarp0) {
+    // offsets of rows (contiguous) or of tokens along K (K-grouped): multiples of 128, in range
+    const int32_t limit = MODE == kKGrouped ? a.KB * BK : a.rows;
     bool bad = false;
     for (int i = lane; i <= a.E; i += 32) {
       const int32_t v = __ldg(a.groups + i);
       table[i] = v;
-      if (v < 0 || (v & (BM - 1)) || v > a.rows) bad = true;
+      if (v < 0 || (v & (BM - 1)) || v > limit) bad = true;
       if (i < a.E && __ldg(a.groups + i + 1) < v) bad = true;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) {
@@ -508,15 +547,18 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
   // a CTA pair walks the tiles of its cluster index; both CTAs see every pair tile
   const int32_t tile0 = PAIR ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
   const int32_t tile_step = PAIR ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
-  auto fetch_tile = [&](int32_t t, Tile& ti) -> bool {
+  // the tile of piece pc; K-grouped tiles cover their expert's K blocks (whole tiles only)
+  auto fetch_tile = [&](Piece& pc, Tile& ti) -> bool {
     if constexpr (PAIR) {
-      get_pair_tile<BN, MODE>(a, table, ptab, t, rank, ti);
+      get_pair_tile<BN, MODE>(a, table, ptab, pc.t, rank, ti);
       return true;
     } else {
-      return get_tile<BN, MODE>(a, table, t, ti);
+      const bool ok = get_tile<BN, MODE>(a, table, pc.t, ti);
+      if (MODE == kKGrouped) pc.kb1 = ti.kb_count;
+      return ok;
     }
   };
-  if (MODE == kContiguous && misc[2]) num_tiles = 0;
+  if ((MODE == kContiguous || MODE == kKGrouped) && misc[2]) num_tiles = 0;
   // stream-K tail: single-CTA tiles with one K part and one issuer only
   const bool sk_on = !PAIR && C::kKSplit == 1 && C::kMmaWarps == 1 && a.sk != 0;
   if (warp < C::kEpiWarp0) {
@@ -543,7 +585,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       Piece pc;
       while (ok && next_piece(w, pc)) {
         Tile ti;
-        if (!fetch_tile(pc.t, ti)) continue;
+        if (!fetch_tile(pc, ti)) continue;
         // the K blocks of a stage past the end of K are zero-filled and never read
         for (int32_t kb = pc.kb0; kb < pc.kb1; kb += KPS, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
@@ -565,8 +607,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
             tma_load_4d_pair(leader, dB, &tmB, fb, 0, ti.n0 + static_cast<int32_t>(rank) * C::kBRows, kb, ti.g);
           } else {
             mbar_arrive_expect_tx(leader, full(s), C::kStageABytes + C::kStageBBytes);
-            tma_load_3d(leader, dA, &tmA, full(s), 0, ti.a_row, kb);
-            tma_load_4d(leader, dB, &tmB, full(s), 0, ti.n0, kb, ti.g);
+            tma_load_3d(leader, dA, &tmA, full(s), 0, ti.a_row, ti.kb_first + kb);
+            tma_load_4d(leader, dB, &tmB, full(s), 0, ti.n0, ti.kb_first + kb, MODE == kKGrouped ? 0 : ti.g);
           }
         }
       }
@@ -580,7 +622,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
       }
     } else if (warp >= 1 && warp <= MW && rank == 0 && (!kLone || leader)) {
       // ---------------------------------------------------------- MMA issuer(s) (rank 0 of a pair)
-      constexpr uint32_t idesc = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN);
+      const uint32_t idesc = idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN) | a.idesc_fmt;
       // descriptors of stage 0; stage s and K step k add (offset in bytes) / 16 to the
       // 14-bit start-address field (shared addresses stay below 2^18, so it cannot carry)
       const uint64_t adesc0 = smem_desc_k_sw128(base + C::kOffA);
@@ -594,7 +636,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         Piece pc;
         while (ok && next_piece(w, pc)) {
           Tile ti;
-          if (!fetch_tile(pc.t, ti)) continue;
+          if (!fetch_tile(pc, ti)) continue;
           const uint32_t b = np % NB, tph = (np / NB) & 1u;
           ++np;
           if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
@@ -627,7 +669,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         Piece pc;
         while (ok && next_piece(w, pc)) {
           Tile ti;
-          if (!fetch_tile(pc.t, ti)) continue;
+          if (!fetch_tile(pc, ti)) continue;
           for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
             const uint32_t s = it % S, ph = (it / S) & 1u;
             const uint32_t b = it % NB, tph = (it / NB) & 1u;
@@ -673,7 +715,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         Piece pc;
         while (ok && next_piece(w, pc)) {
           Tile ti;
-          if (!fetch_tile(pc.t, ti)) continue;
+          if (!fetch_tile(pc, ti)) continue;
           for (int32_t kb0 = 0; kb0 < a.KB && ok; kb0 += KPS, ++it) {
             const int32_t left = a.KB - kb0;
             const uint32_t nk = static_cast<uint32_t>(left < KPS ? left : KPS);
@@ -753,7 +795,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
     Piece pc;
     while (ok && next_piece(w, pc)) {
       Tile ti;
-      if (!fetch_tile(pc.t, ti)) continue;
+      if (!fetch_tile(pc, ti)) continue;
       const int32_t ncol0 = ti.n0 + col0;
       const bool has_cols = ncol0 < a.N;
       // small-M tiles: warps whose rows are all past M skip the promotion (nothing to store)
@@ -781,15 +823,17 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         __syncwarp();
         release_tmem(b);
       } else {
+        // (K-grouped: the B scales are one per column and K block, read per K block below)
+        const bool blk_sb = MODE != kKGrouped && has_cols;
         const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
         // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
         // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
         int32_t sb_base = pc.kb0 & ~31;
-        float sb_cur = (has_cols && sb_base + lane < a.KB) ? ld_nc_f32(sbp + sb_base + lane) : 0.0f;
-        float sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
+        float sb_cur = (blk_sb && sb_base + lane < a.KB) ? ld_nc_f32(sbp + sb_base + lane) : 0.0f;
+        float sb_nxt = (blk_sb && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
         // A-row scale of this thread's row, read from global memory kSAAhead K-block steps
         // before use (coalesced: a warp reads 32 consecutive rows of one K block)
-        const float* sap = a.sA + grow;
+        const float* sap = a.sA + static_cast<int64_t>(ti.kb_first) * a.ld_sa + grow;
         float sa_q[kSAAhead];
 #pragma unroll
         for (int i = 0; i < kSAAhead; ++i) {
@@ -798,7 +842,30 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         }
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+        // K-grouped: the B scales of this warp's columns for one K block, lane l loading columns
+        // 4l .. 4l+3 (one coalesced 16-byte load per lane, a K block ahead).  They are staged in
+        // the first 512 bytes of this warp's output box (idle until the tile's store; the previous
+        // tile's store must have finished reading it) and read back with warp-uniform addresses.
+        if (MODE == kKGrouped) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
+        auto load_sbv = [&](int32_t kbi) {
+          float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (MODE == kKGrouped && kbi < pc.kb1 && ncol0 + 4 * lane < a.N)
+            r = __ldg(reinterpret_cast<const float4*>(a.sB + static_cast<int64_t>(ti.kb_first + kbi) * a.ld_sb +
+                                                      ncol0) + lane);
+          return r;
+        };
+        float4 sbv_nxt = load_sbv(pc.kb0 + kpart);
         for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += C::kKSplit) {
+          if (MODE == kKGrouped) {
+            __syncwarp();  // every lane has read the previous K block's scales
+            st_shared_v4(out_addr + 16 * lane, __float_as_uint(sbv_nxt.x), __float_as_uint(sbv_nxt.y),
+                         __float_as_uint(sbv_nxt.z), __float_as_uint(sbv_nxt.w));
+            __syncwarp();
+          }
+          sbv_nxt = load_sbv(kb + C::kKSplit);
           const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
           const uint32_t b = it % NB, tph = (it / NB) & 1u;
           const float sa_kb = sa_q[0];
@@ -812,7 +879,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
           if (kb >= sb_base + 32) {
             sb_base += 32;
             sb_cur = sb_nxt;
-            sb_nxt = (has_cols && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
+            sb_nxt = (blk_sb && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
           }
           const float sb_kb = __shfl_sync(0xffffffffu, sb_cur, kb - sb_base);
           const float scale = sa_kb * sb_kb;
@@ -831,9 +898,23 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
                 __syncwarp();
                 release_tmem(b);
               }
+              if constexpr (MODE == kKGrouped) {
+                // one B scale per column: s[n] = sa * sB[kb][n]
+                const float2 sa2 = make_float2(sa_kb, sa_kb);
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+                for (int i = 0; i < 16; ++i) {
+                  const float4 s4 = ld_shared_v4f(out_addr + 16 * (c * 16 + i));
+                  const float2 s01 = __fmul2_rn(sa2, make_float2(s4.x, s4.y));
+                  const float2 s23 = __fmul2_rn(sa2, make_float2(s4.z, s4.w));
+                  acc[c * 32 + 2 * i] = __ffma2_rn(make_float2(v[4 * i], v[4 * i + 1]), s01, acc[c * 32 + 2 * i]);
+                  acc[c * 32 + 2 * i + 1] =
+                      __ffma2_rn(make_float2(v[4 * i + 2], v[4 * i + 3]), s23, acc[c * 32 + 2 * i + 1]);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+              }
             }
           } else {
             tc_fence_before();
@@ -928,7 +1009,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
           for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(sc, sc));
         }
       }
-      if (MODE != kMasked || nvalid == 32) {
+      if ((MODE != kMasked && MODE != kKGrouped) || nvalid == 32) {
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 32; ++j) {
           if (ncol0 + 32 * j >= a.N) break;
@@ -947,13 +1028,14 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmD, out_addr, ncol0 + 32 * j, ti.a_row + q * 32);
+            tma_store_2d(&tmD, out_addr, ncol0 + 32 * j, ti.d_row + q * 32);
             bulk_commit();
           }
         }
       } else if (lane < nvalid) {
-        // partial rows of a masked expert: plain stores, row by row
-        __nv_bfloat16* drow = a.D + static_cast<int64_t>(ti.a_row + q * 32 + lane) * a.ldd + ncol0;
+        // partial rows (a masked expert's count, the last rows of a K-grouped expert's matrix):
+        // plain stores, row by row
+        __nv_bfloat16* drow = a.D + static_cast<int64_t>(ti.d_row + q * 32 + lane) * a.ldd + ncol0;
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 8; ++j) {
           if (ncol0 + 8 * j < a.N) {
@@ -1188,6 +1270,8 @@ struct Operands {
   int64_t rows, N, K, E, cap;
   const int32_t* groups;
   int32_t sa_step = 0, sb_step = 0;  // epilogue-scaled variant only
+  uint32_t idesc_fmt = 0;             // operand formats (A e5m2: 1 << 7)
+  int64_t ld_sb = 0;                  // kKGrouped: B scales [K blocks][ld_sb]
 };
 
 // EPI: the epilogue-scaled variant (per-tensor / per-token / per-channel scales)
@@ -1198,13 +1282,15 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   if (st != FP8G_OK) return st;
   if (o.rows == 0) return FP8G_OK;
 
-  const int64_t m_blocks = (MODE == kMasked) ? o.E * ((o.cap + BM - 1) / BM) : (o.rows + BM - 1) / BM;
-  int bn = choose_block_n(m_blocks, o.N, dev->sm_count, EPI ? 128 : 64);
+  const int64_t m_blocks = (MODE == kMasked)     ? o.E * ((o.cap + BM - 1) / BM)
+                           : (MODE == kKGrouped) ? o.E * ((o.rows + BM - 1) / BM)
+                                                 : (o.rows + BM - 1) / BM;
+  int bn = choose_block_n(m_blocks, o.N, dev->sm_count, (EPI || MODE == kKGrouped) ? 128 : 64);
   // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
   const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
   // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2); the epilogue-scaled variant has single-CTA tiles
-  const int pmode = EPI ? 0 : env_pair();
+  const int pmode = (EPI || MODE == kKGrouped) ? 0 : env_pair();
   const bool pair = bn == 256 && pmode != 0 &&
                     (MODE != kDense || (o.rows + BM - 1) / BM >= 2) && dev->sm_count >= 2;
   if (pair && pmode == 2) bn = 128;
@@ -1229,6 +1315,9 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   a.budget = wait_budget_cycles();
   a.sa_step = o.sa_step;
   a.sb_step = o.sb_step;
+  a.idesc_fmt = o.idesc_fmt;
+  a.ld_sb = o.ld_sb;
+  if (MODE == kKGrouped) a.num_tiles = static_cast<int32_t>(o.E) * a.num_m * a.num_n;
 
   // K blocks per stage of the variant launched below (its Cfg::kKPS)
   const uint32_t kps = small_m ? Cfg<64, true>::kKPS : 1u;
@@ -1245,7 +1334,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   {
     // B as [E][K/128][N][128]
     const uint64_t dims[4] = {BK, static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.K / BK),
-                              static_cast<uint64_t>(o.E)};
+                              static_cast<uint64_t>(MODE == kKGrouped ? 1 : o.E)};
     const uint64_t strides[3] = {static_cast<uint64_t>(o.ldb), BK, static_cast<uint64_t>(o.ldb * o.N)};
     const uint32_t box[4] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn), kps, 1};
     if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, o.B, dims, strides, box,
@@ -1253,7 +1342,9 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
       return st;
   }
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.rows)};
+    // D: [rows, N] (K-grouped: one [rows, N] matrix per expert, stacked)
+    const uint64_t d_rows = static_cast<uint64_t>(MODE == kKGrouped ? o.E * o.rows : o.rows);
+    const uint64_t dims[2] = {static_cast<uint64_t>(o.N), d_rows};
     const uint64_t strides[1] = {static_cast<uint64_t>(o.ldd * 2)};
     const uint32_t box[2] = {32, 32};
     if ((st = encode_tmap(&tD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.D, dims, strides, box,
@@ -1279,7 +1370,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
     if (u < umin) u = umin;
     return U > 0 && KB - u >= a.sk_min_gain;
   };
-  if (!pair && !small_m && bn >= 128 && env_streamk() &&
+  if (MODE != kKGrouped && !pair && !small_m && bn >= 128 && env_streamk() &&
       (MODE == kMasked || tail_splits(a.num_tiles))) {
     int dev_id = 0;
     cudaGetDevice(&dev_id);
@@ -1313,40 +1404,48 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
 
   t_last_bn = bn;
   t_last_grid = grid;
-  if constexpr (EPI) {
+  if constexpr (MODE == kKGrouped) {
+    if (bn == 256) {
+      t_last_stages = Cfg<256>::kStages;
+      return launch_kernel<256, kKGrouped>(a, tA, tB, tD, grid, table_entries, stream);
+    }
+    t_last_stages = Cfg<128>::kStages;
+    return launch_kernel<128, kKGrouped>(a, tA, tB, tD, grid, table_entries, stream);
+  } else if constexpr (EPI) {
     if (bn == 256) {
       t_last_stages = Cfg<256>::kStages;
       return launch_kernel<256, MODE, false, true>(a, tA, tB, tD, grid, table_entries, stream);
     }
     t_last_stages = Cfg<128>::kStages;
     return launch_kernel<128, MODE, false, true>(a, tA, tB, tD, grid, table_entries, stream);
-  }
-  switch (bn) {
-    case 256:
-      if (pair) {
-        t_last_stages = Cfg<256, false, true>::kStages;
-        return launch_kernel<256, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
-                                                                               table_entries, stream);
-      }
-      t_last_stages = Cfg<256>::kStages;
-      return launch_kernel<256, MODE>(a, tA, tB, tD, grid, table_entries, stream);
-    case 128:
-      if (pair) {
-        t_last_stages = Cfg<128, false, true>::kStages;
-        return launch_kernel<128, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
-                                                                               table_entries, stream);
-      }
-      t_last_stages = Cfg<128>::kStages;
-      return launch_kernel<128, MODE>(a, tA, tB, tD, grid, table_entries, stream);
-    default:
-      if constexpr (MODE == kDense) {
-        if (small_m) {
-          t_last_stages = Cfg<64, true>::kStages;
-          return launch_kernel<64, kDenseSmallM>(a, tA, tB, tD, grid, table_entries, stream);
+  } else {
+    switch (bn) {
+      case 256:
+        if (pair) {
+          t_last_stages = Cfg<256, false, true>::kStages;
+          return launch_kernel<256, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
+                                                                                 table_entries, stream);
         }
-      }
-      t_last_stages = Cfg<64>::kStages;
-      return launch_kernel<64, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+        t_last_stages = Cfg<256>::kStages;
+        return launch_kernel<256, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+      case 128:
+        if (pair) {
+          t_last_stages = Cfg<128, false, true>::kStages;
+          return launch_kernel<128, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
+                                                                                 table_entries, stream);
+        }
+        t_last_stages = Cfg<128>::kStages;
+        return launch_kernel<128, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+      default:
+        if constexpr (MODE == kDense) {
+          if (small_m) {
+            t_last_stages = Cfg<64, true>::kStages;
+            return launch_kernel<64, kDenseSmallM>(a, tA, tB, tD, grid, table_entries, stream);
+          }
+        }
+        t_last_stages = Cfg<64>::kStages;
+        return launch_kernel<64, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+    }
   }
 }
 
@@ -1427,6 +1526,63 @@ extern "C" int fp8_grouped_gemm_masked(const void* A, const float* sA, int64_t l
     return FP8G_ERR_ALIGNMENT;
   Operands o{A, K, sA, ld_sa, B, K, sB, D, N, static_cast<int64_t>(E) * cap, N, K, E, cap, masked_m};
   return run_gemm<kMasked>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_gemm_nt_dgrad(const void* A, int64_t lda, const float* sA, int64_t ld_sa,
+                                 const void* B, int64_t ldb, const float* sB, void* D, int64_t ldd,
+                                 int64_t M, int64_t N, int64_t K, void* stream) {
+  // the argument rules of fp8_gemm_nt; A holds e5m2 codes
+  if (M < 0 || M > kMaxI32 || N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 ||
+      K > kMaxI32)
+    return FP8G_ERR_INVALID_ARG;
+  if (lda < K || ldb < K || ldd < N || ld_sa < M) return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;
+  if (!A || !sA || !B || !sB || !D) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0 || ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr};
+  o.idesc_fmt = 1u << 7;  // A: e5m2
+  return run_gemm<kDense>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_contiguous_dgrad(const void* A, const float* sA, int64_t ld_sa,
+                                                 const void* B, const float* sB, void* D,
+                                                 const int32_t* group_offsets, int32_t E,
+                                                 int64_t M_total, int64_t N, int64_t K, void* stream) {
+  // the argument rules of fp8_grouped_gemm_contiguous; A holds e5m2 codes
+  if (E < 1 || E > kMaxExperts || M_total < 0 || M_total > kMaxI32 || M_total % 128 != 0 ||
+      N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 || K > kMaxI32 ||
+      ld_sa < M_total)
+    return FP8G_ERR_INVALID_ARG;
+  if (M_total == 0) return FP8G_OK;
+  if (!A || !sA || !B || !sB || !D || !group_offsets) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      (reinterpret_cast<uintptr_t>(group_offsets) & 3u) || ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, K, sA, ld_sa, B, K, sB, D, N, M_total, N, K, E, 0, group_offsets};
+  o.idesc_fmt = 1u << 7;  // A: e5m2
+  return run_gemm<kContiguous>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_wgrad(const void* A, int64_t lda, const float* sA, int64_t ld_sa,
+                                      const void* B, int64_t ldb, const float* sB, int64_t ld_sb,
+                                      void* D, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
+                                      int64_t T, void* stream) {
+  if (E < 1 || E > kMaxExperts || M < 0 || M % 16 != 0 || static_cast<int64_t>(E) * M > kMaxI32 ||
+      N <= 0 || N > kMaxI32 || N % 16 != 0 || T <= 0 || T % 128 != 0 || T > kMaxI32 || lda < T ||
+      ldb < T || ld_sa < M || ld_sb < N)
+    return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;
+  if (!A || !sA || !B || !sB || !D || !offsets) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
+      lda % 16 != 0 || ldb % 16 != 0 || ld_sa % 4 != 0 || ld_sb % 4 != 0 ||
+      (reinterpret_cast<uintptr_t>(offsets) & 3u))
+    return FP8G_ERR_ALIGNMENT;
+  Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, N, M, N, T, E, 0, offsets};
+  o.idesc_fmt = 1u << 7;  // A (the output gradient): e5m2
+  o.ld_sb = ld_sb;
+  return run_gemm<kKGrouped>(o, static_cast<cudaStream_t>(stream));
 }
 
 // Epilogue-scaled forms: the scale arguments are checked here, the rest as in the block-scaled

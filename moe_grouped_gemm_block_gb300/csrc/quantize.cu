@@ -21,6 +21,7 @@ namespace fp8g {
 namespace {
 
 constexpr float kE4M3Max = 448.0f;
+constexpr float kE5M2Max = 57344.0f;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -58,6 +59,22 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, flo
       : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
   return w;
 }
+// The same for e5m2 (gradients: 1-5-2 bits, largest finite value 57344).
+__device__ __forceinline__ uint32_t cvt_e5m2x4(float a0, float a1, float a2, float a3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(w)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return w;
+}
+enum CodeFormat : int { kE4M3 = 0, kE5M2 = 1 };
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_x4(float a0, float a1, float a2, float a3) {
+  return FMT == kE5M2 ? cvt_e5m2x4(a0, a1, a2, a3) : cvt_e4m3x4(a0, a1, a2, a3);
+}
 
 // Direct path.  For most blocks the single product y = RN(x * RN(1/s)) already has the code of
 // RN(x / s) for every bf16 x with |x| <= amax, and no bracket is needed.  Whether it does depends
@@ -77,7 +94,9 @@ __device__ __forceinline__ bool direct_ok(float amax, float s) {
   return s >= 1.17549435e-38f && ((word >> (a7 & 31u)) & 1u) != 0u;
 }
 
-template <int N>
+// FMT e5m2: the bracket argument holds for any monotone round-to-nearest conversion; the direct
+// path's table is e4m3's, so e5m2 callers pass direct = false.
+template <int N, int FMT = kE4M3>
 __device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direct, uint32_t (&w)[N / 4]) {
   static_assert(N % 4 == 0, "N");
   if (s == 0.0f) {
@@ -93,7 +112,7 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direc
     for (int i = 0; i < N / 4; ++i) {
       const float2 y01 = __fmul2_rn(make_float2(f[4 * i], f[4 * i + 1]), r2);
       const float2 y23 = __fmul2_rn(make_float2(f[4 * i + 2], f[4 * i + 3]), r2);
-      w[i] = cvt_e4m3x4(y01.x, y01.y, y23.x, y23.y);
+      w[i] = cvt_x4<FMT>(y01.x, y01.y, y23.x, y23.y);
     }
     return;
   }
@@ -107,15 +126,15 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direc
       const float2 x01 = make_float2(f[4 * i], f[4 * i + 1]), x23 = make_float2(f[4 * i + 2], f[4 * i + 3]);
       const float2 l01 = __fmul2_rn(x01, rlo), l23 = __fmul2_rn(x23, rlo);
       const float2 h01 = __fmul2_rn(x01, rhi), h23 = __fmul2_rn(x23, rhi);
-      w[i] = cvt_e4m3x4(l01.x, l01.y, l23.x, l23.y);
-      diff |= w[i] ^ cvt_e4m3x4(h01.x, h01.y, h23.x, h23.y);
+      w[i] = cvt_x4<FMT>(l01.x, l01.y, l23.x, l23.y);
+      diff |= w[i] ^ cvt_x4<FMT>(h01.x, h01.y, h23.x, h23.y);
     }
     exact = diff != 0u;  // rare: some element sits within 2^-20 of a decision point
   }
   if (exact) {
 #pragma unroll
     for (int i = 0; i < N / 4; ++i)
-      w[i] = cvt_e4m3x4(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s), __fdiv_rn(f[4 * i + 2], s),
+      w[i] = cvt_x4<FMT>(__fdiv_rn(f[4 * i], s), __fdiv_rn(f[4 * i + 1], s), __fdiv_rn(f[4 * i + 2], s),
                         __fdiv_rn(f[4 * i + 3], s));
   }
 }
@@ -133,7 +152,8 @@ constexpr int kQThreads = 256;
 constexpr int kQUnroll = 2;
 
 // GATHER: output row m holds input row row_src[m] (a zero row where row_src[m] < 0).
-template <bool GATHER>
+// FMT: e4m3 (s = amax / 448) or e5m2 (gradients, s = amax / 57344).
+template <bool GATHER, int FMT = kE4M3>
 __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa,
@@ -173,10 +193,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
       // reduce over the 8 lanes of this group (xor offsets < 8 stay inside it)
 #pragma unroll
       for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-      const float s = __fdiv_rn(a, kE4M3Max);
+      const float s = __fdiv_rn(a, FMT == kE5M2 ? kE5M2Max : kE4M3Max);
       if (base + u * n_groups < total) {
         uint32_t c[4];
-        quant_n<16>(f, s, direct_ok(a, s), c);
+        quant_n<16, FMT>(f, s, FMT == kE4M3 && direct_ok(a, s), c);
         uint8_t* dst = q + m[u] * ldq + kb[u] * 128 + sub * 8;
         *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
         *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
@@ -540,6 +560,31 @@ extern "C" int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t l
   if (blocks > cap) blocks = cap;
   quantize_1x128_kernel<false><<<static_cast<unsigned>(blocks), kQThreads, 0,
                                  static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx,
+      static_cast<uint8_t*>(q), ldq, sA, ld_sa, nullptr);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+extern "C" int fp8_quantize_1x128_e5m2(const void* x, int64_t M, int64_t K, int64_t ldx, void* q,
+                                       int64_t ldq, float* sA, int64_t ld_sa, void* stream) {
+  if (M < 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq < K || ld_sa < M)
+    return FP8G_ERR_INVALID_ARG;
+  if (M == 0) return FP8G_OK;
+  if (!x || !q || !sA) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sA) || ldx % 8 != 0 || ldq % 16 != 0 ||
+      ld_sa % 4 != 0)
+    return FP8G_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  const int64_t items = M * (K / 128);
+  if (items >= (int64_t{1} << 31) || M > 0x7FFFFFFF) return FP8G_ERR_INVALID_ARG;
+  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  int64_t blocks = (items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
+  if (blocks > cap) blocks = cap;
+  quantize_1x128_kernel<false, kE5M2><<<static_cast<unsigned>(blocks), kQThreads, 0,
+                                        static_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx,
       static_cast<uint8_t*>(q), ldq, sA, ld_sa, nullptr);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;

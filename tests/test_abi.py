@@ -171,3 +171,28 @@ def test_quantise_per_row_and_per_tensor_validation(lib):
     assert t(P, 1, 4, 128, 128, P, 128, None, None) == INVALID
     assert t(P, 1, 4, 128, 128, P, 128, P + 2, None) == ALIGN
     assert t(P, 1, 1 << 28, 128, 128, P, 128, P, None) == INVALID  # M * K / 8 >= 2^31
+
+
+def test_backward_entry_points_validation(lib):
+    q = lib.fp8_quantize_1x128_e5m2
+    assert q(P, 4, 100, 128, P, 128, P, 4, None) == INVALID          # K % 128
+    assert q(P, 8, 128, 128, P, 128, P, 4, None) == INVALID          # ld_sa < M
+    assert q(P + 8, 4, 128, 128, P, 128, P, 4, None) == ALIGN
+    assert q(P, 0, 128, 128, None, 128, None, 4, None) == 0           # M == 0: no-op
+    assert lib.fp8_gemm_nt_dgrad(*_nt(K=200)) == INVALID
+    assert lib.fp8_gemm_nt_dgrad(*_nt(A=P + 1)) == ALIGN
+    assert lib.fp8_gemm_nt_dgrad(*_nt(M=0, A=None, sA=None, B=None, sB=None, D=None)) == 0
+    c = lib.fp8_grouped_gemm_contiguous_dgrad
+    assert c(P, P, 256, P, P, P, P, 2, 200, 256, 256, None) == INVALID  # M_total % 128
+    assert c(P, P, 256, P, P, P, P + 2, 2, 256, 256, 256, None) == ALIGN
+    w = lib.fp8_grouped_gemm_wgrad
+    # (A, lda, sA, ld_sa, B, ldb, sB, ld_sb, D, offsets, E, M, N, T, stream)
+    assert w(P, 256, P, 64, P, 256, P, 256, P, P, 2, 64, 256, 200, None) == INVALID   # T % 128
+    assert w(P, 256, P, 64, P, 256, P, 256, P, P, 2, 72, 256, 256, None) == INVALID   # M % 16
+    assert w(P, 256, P, 32, P, 256, P, 256, P, P, 2, 64, 256, 256, None) == INVALID   # ld_sa < M
+    assert w(P, 256, P, 64, P, 256, P, 128, P, P, 2, 64, 256, 256, None) == INVALID   # ld_sb < N
+    assert w(P, 128, P, 64, P, 256, P, 256, P, P, 2, 64, 256, 256, None) == INVALID   # lda < T
+    assert w(P, 256, P, 64, P, 256, P, 256, P, P, 0, 64, 256, 256, None) == INVALID   # E
+    assert w(P, 256, P, 64, P, 256, P, 256, P, P + 2, 2, 64, 256, 256, None) == ALIGN
+    assert w(P, 256, P, 66, P, 256, P, 256, P, P, 2, 64, 256, 256, None) == ALIGN     # ld_sa % 4
+    assert w(P, 256, P, 64, P, 256, P, 256, P, P, 2, 0, 256, 256, None) == 0          # M == 0: no-op
