@@ -538,10 +538,10 @@ def _rel_fro(outs, D, pieces):
 
 
 # torch._scaled_mm is not called: with the installed torch on sm_103 its block-scaled (1x128 / 128x128)
-# form returns CUBLAS_STATUS_NOT_SUPPORTED, and its rowwise form ended in "unspecified launch failure".
+# form is not supported by cuBLASLt, and a call of its rowwise form left the CUDA context unusable.
 VENDOR_FP8_NOTE = ("not run: torch._scaled_mm with 1x128/128x128 block scales is not supported on sm_103 with "
-                   "the installed torch (CUBLAS_STATUS_NOT_SUPPORTED), and its rowwise form failed there with "
-                   "an unspecified launch failure")
+                   "the installed torch (cuBLASLt reports the configuration unsupported), and a call of its "
+                   "rowwise form left the CUDA context unusable")
 
 
 def measure_library_rows(cases, flush, fp8_peak, breakdown, reps=20):
