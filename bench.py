@@ -413,6 +413,8 @@ def measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak, reps=20):
     out = {}
     if "large_4096x8192" in names:
         out.update(measure_scaled_rows(g, dev, flush, hbm_peak, fp8_peak, reps))
+    if "moe_masked" in names:
+        out.update(measure_masked_scaled_row(g, dev, flush, hbm_peak, fp8_peak, reps))
     if "moe_contiguous" not in names:
         return out
     w = WORKLOADS["moe_contiguous"]
@@ -470,6 +472,33 @@ def measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak, reps=20):
     del qa, qb, D
     out.update(measure_backward_rows(g, dev, flush, hbm_peak, fp8_peak, inp, w, reps))
     return out
+
+
+def measure_masked_scaled_row(g, dev, flush, hbm_peak, fp8_peak, reps):
+    """The epilogue-scaled masked GEMM (per-token x per-channel) on the MoE masked workload: the same
+    weight stream as the block-scaled masked GEMM without its per-K-block promotion."""
+    w = WORKLOADS["moe_masked"]
+    inp = make_inputs(w, dev)
+    A, B, cnt = inp["A"], inp["B"], inp["masked_m"]
+    E, cap, K = A.shape
+    N = B.shape[1]
+    qa, sa = g.quantize_per_row(A.reshape(E * cap, K))
+    qb, sb = g.quantize_per_row(B.reshape(E * N, K))
+    del inp, B
+    masked = cnt.to(dev)
+    D = torch.empty((E, cap, N), dtype=torch.bfloat16, device=dev)
+    qa3, qb3, sb2 = qa.reshape(E, cap, K), qb.reshape(E, N, K), sb.reshape(E, N)
+    us = _time_calls(lambda: g.fp8_grouped_gemm_masked_scaled(qa3, sa, qb3, sb2, D, masked), flush, reps)
+    rows = int(cnt.sum())
+    active = int((cnt > 0).sum())
+    flops = 2.0 * rows * N * K
+    nbytes = rows * K + active * N * K + 2 * rows * N
+    tf = flops / (us * 1e-6) / 1e12
+    return {"grouped_gemm_masked_scaled": {
+        "workload": f"moe_masked, per-token A x per-channel B: E={E}, cap={cap}, N={N}, K={K}, rows={rows}",
+        "us": round(us, 2), "tflops": round(tf, 1), "pct_fp8_peak": round(100 * tf / fp8_peak, 1),
+        "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+        "pct_hbm_peak": round(100 * nbytes / (us * 1e-6) / 1e9 / hbm_peak, 1), "launches": 1}}
 
 
 def measure_backward_rows(g, dev, flush, hbm_peak, fp8_peak, inp, w, reps):
