@@ -200,8 +200,10 @@ class Case:
             self.D = torch.empty((w.E, w.cap, w.N), dtype=torch.bfloat16, device=dev)
             self.meta = inp["masked_m"].to(dev)
         self.masked_rows = int(inp["masked_m"].sum()) if w.kind == "masked" else None
-        # algorithmic bytes: quantise reads bf16 A, writes e4m3 A + scales
-        self.q_bytes = self.rows * w.K * 3 + self.rows * (w.K // 128) * 4
+        # algorithmic bytes: quantise reads bf16 A, writes e4m3 A + scales (masked: the valid rows,
+        # the only ones the masked quantiser touches)
+        q_rows = self.masked_rows if w.kind == "masked" else self.rows
+        self.q_bytes = q_rows * w.K * 3 + q_rows * (w.K // 128) * 4
         self.gemm_bytes = self._gemm_bytes()
 
     def _gemm_bytes(self) -> float:
@@ -217,7 +219,13 @@ class Case:
         return m * w.K + active * w.N * w.K + 4 * (m * kb + active * nbs * kb) + 2 * m * w.N
 
     def quantize(self, A=None):
-        self.g.fp8_quantize_1x128(self.A if A is None else A, self.qA, self.sA)
+        A = self.A if A is None else A
+        if self.w.kind == "masked":  # only each expert's valid rows
+            w = self.w
+            self.g.fp8_quantize_1x128_masked(A.view(w.E, w.cap, w.K), self.qA.view(w.E, w.cap, w.K), self.sA,
+                                             self.meta)
+        else:
+            self.g.fp8_quantize_1x128(A, self.qA, self.sA)
 
     def gemm(self, D=None):
         g, w = self.g, self.w

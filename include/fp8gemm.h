@@ -86,6 +86,23 @@ int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, void* q
                        float* sA, int64_t ld_sa, void* stream);
 
 /*
+ * fp8_quantize_1x128_masked -- fp8_quantize_1x128 for the masked layout: x and q are [E, cap, K]
+ * (contiguous), and only rows m < masked_m[e] of each expert are quantised -- the rows
+ * fp8_grouped_gemm_masked reads for its output.  The other rows of q and their scales are left
+ * as they are (each output row of the masked GEMM depends only on its own row of A and its
+ * scales, and rows past the count are never stored).
+ *
+ *   x         bf16 [E, cap, K], contiguous
+ *   masked_m  int32 [E], DEVICE memory; values are clamped to [0, cap]
+ *   q         e4m3 [E, cap, K], contiguous
+ *   sA        fp32 [K/128][ld_sa] with row index e*cap + m (ld_sa >= E*cap, ld_sa % 4 == 0)
+ *   1 <= E <= 65535, cap >= 0 (cap == 0: no-op), K % 128 == 0, E*cap*(K/128) < 2^31.  x, q, sA 16-byte
+ *   aligned.
+ */
+int fp8_quantize_1x128_masked(const void* x, int32_t E, int64_t cap, int64_t K, const int32_t* masked_m,
+                              void* q, float* sA, int64_t ld_sa, void* stream);
+
+/*
  * fp8_route_gather_quantize_1x128 -- builds the contiguous grouped layout that
  * fp8_grouped_gemm_contiguous reads, straight from routed tokens, and quantises it
  * ("DeepGEMM explainer" sec. 3.2 and 4.2; "DeepGEMM FP8 walk-through" sec. 5.3:

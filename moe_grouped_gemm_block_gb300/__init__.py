@@ -14,6 +14,7 @@ functions here carry the same names and take torch tensors:
     fp8_gemm_nt_scaled(A, sA, B, sB, D)                  epilogue scales: sA [M] or [1], sB [N] or [1]
     fp8_grouped_gemm_contiguous_scaled(A, sA, B, sB, D, group_offsets)   sB [E,N] or [E]
     fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m)
+    fp8_quantize_1x128_masked(x, q, sA, masked_m)      masked layout: only each expert's valid rows
     fp8_quantize_1x128_e5m2(x, q, sA)                  gradients: e5m2 codes, s = amax / 57344
     fp8_gemm_nt_dgrad(A, sA, B, sB, D)                 data gradient: A e5m2 [M,K], B e4m3 [N,K] (= W^T)
     fp8_grouped_gemm_contiguous_dgrad(A, sA, B, sB, D, group_offsets)   grouped data gradient
@@ -67,6 +68,7 @@ _SIGNATURES = {
     "fp8_gemm_nt_scaled": [_P, _I64, _FP, _I32, _P, _I64, _FP, _I32, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_contiguous_scaled": [_P, _FP, _I32, _P, _FP, _I32, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_masked_scaled": [_P, _FP, _I32, _P, _FP, _I32, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8_quantize_1x128_masked": [_P, _I32, _I64, _I64, _P, _P, _FP, _I64, _P],
     "fp8_quantize_1x128_e5m2": [_P, _I64, _I64, _I64, _P, _I64, _FP, _I64, _P],
     "fp8_gemm_nt_dgrad": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_contiguous_dgrad": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
@@ -267,6 +269,19 @@ def fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m) -> None:
     _check(lib().fp8_grouped_gemm_masked_scaled(_ptr(A), _ptr(sA), pa, _ptr(B), _ptr(sB), pb, _ptr(D),
                                                 _ptr(masked_m), E, cap, N, K, _stream(A)),
            "fp8_grouped_gemm_masked_scaled")
+
+
+def fp8_quantize_1x128_masked(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor, masked_m: torch.Tensor) -> None:
+    """x bf16 [E,cap,K] -> q e4m3 [E,cap,K], sA f32 [K/128, ld_sa >= E*cap]: only rows m < masked_m[e]."""
+    _need(x.dtype == torch.bfloat16 and x.dim() == 3 and x.is_contiguous(), "x: bf16 [E,cap,K] contiguous")
+    _need(_is_fp8(q) and q.shape == x.shape and q.is_contiguous(), "q: e4m3 [E,cap,K] contiguous")
+    _need(masked_m.dtype == torch.int32 and masked_m.is_cuda, "masked_m: int32 device tensor")
+    E, cap, K = x.shape
+    _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1,
+          "sA: f32 [K/128, ld_sa]")
+    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _check(lib().fp8_quantize_1x128_masked(_ptr(x), E, cap, K, _ptr(masked_m), _ptr(q), _ptr(sA), ld_sa,
+                                           _stream(x)), "fp8_quantize_1x128_masked")
 
 
 def fp8_quantize_1x128_e5m2(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor) -> None:

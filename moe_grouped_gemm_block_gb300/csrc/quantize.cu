@@ -153,27 +153,39 @@ constexpr int kQUnroll = 2;
 
 // GATHER: output row m holds input row row_src[m] (a zero row where row_src[m] < 0).
 // FMT: e4m3 (s = amax / 448) or e5m2 (gradients, s = amax / 57344).
-template <bool GATHER, int FMT = kE4M3>
+// MASKED: rows are experts x cap and only rows r < row_src[e] of expert e (its count, clamped to
+// [0, cap]) are quantised; the others are left as they are.  Grid row blockIdx.y is expert e,
+// striding over that expert's valid (row, K block) items only.
+template <bool GATHER, int FMT = kE4M3, bool MASKED = false>
 __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa,
-    const int32_t* __restrict__ row_src) {
+    const int32_t* __restrict__ row_src, uint32_t cap = 0) {
   const int sub = threadIdx.x & 7;
   const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) >> 3;
   const uint32_t n_groups = gridDim.x * (kQThreads >> 3);
-  const uint32_t total = M * KB;  // the host guarantees M * KB < 2^31
+  uint32_t total = M * KB;  // the host guarantees M * KB < 2^31
+  uint32_t row0 = 0;        // MASKED: the expert's first row
+  if (MASKED) {
+    const int32_t cnt = __ldg(row_src + blockIdx.y);
+    total = static_cast<uint32_t>(min(max(cnt, 0), static_cast<int32_t>(cap))) * KB;
+    row0 = blockIdx.y * cap;
+  }
   for (uint32_t base = group; base - group < total; base += n_groups * kQUnroll) {
     uint4 raw[kQUnroll][2];
     uint32_t m[kQUnroll], kb[kQUnroll];
+    bool live[kQUnroll];
 #pragma unroll
     for (int u = 0; u < kQUnroll; ++u) {
       const uint32_t item = base + u * n_groups;
       m[u] = item / KB;
       kb[u] = item - m[u] * KB;
+      m[u] += row0;
       raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
+      live[u] = item < total;
       int64_t src_row = m[u];
-      if (GATHER && item < total) src_row = __ldg(row_src + m[u]);
-      if (item < total && src_row >= 0) {
+      if (GATHER && live[u]) src_row = __ldg(row_src + m[u]);
+      if (live[u] && src_row >= 0) {
         const __nv_bfloat16* src = x + src_row * ldx + kb[u] * 128 + sub * 8;
         raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
         raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 64));
@@ -194,7 +206,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
 #pragma unroll
       for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
       const float s = __fdiv_rn(a, FMT == kE5M2 ? kE5M2Max : kE4M3Max);
-      if (base + u * n_groups < total) {
+      if (live[u]) {
         uint32_t c[4];
         quant_n<16, FMT>(f, s, FMT == kE4M3 && direct_ok(a, s), c);
         uint8_t* dst = q + m[u] * ldq + kb[u] * 128 + sub * 8;
@@ -562,6 +574,35 @@ extern "C" int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t l
                                  static_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx,
       static_cast<uint8_t*>(q), ldq, sA, ld_sa, nullptr);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+extern "C" int fp8_quantize_1x128_masked(const void* x, int32_t E, int64_t cap, int64_t K,
+                                         const int32_t* masked_m, void* q, float* sA, int64_t ld_sa,
+                                         void* stream) {
+  if (E < 1 || cap < 0 || K <= 0 || K % 128 != 0 || static_cast<int64_t>(E) * cap > 0x7FFFFFFF ||
+      ld_sa < static_cast<int64_t>(E) * cap)
+    return FP8G_ERR_INVALID_ARG;
+  if (cap == 0) return FP8G_OK;
+  if (!x || !q || !sA || !masked_m) return FP8G_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sA) || ld_sa % 4 != 0 ||
+      (reinterpret_cast<uintptr_t>(masked_m) & 3u))
+    return FP8G_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  const int64_t M = static_cast<int64_t>(E) * cap;
+  const int64_t items = M * (K / 128);
+  if (items >= (int64_t{1} << 31) || E > 65535) return FP8G_ERR_INVALID_ARG;
+  // one grid row per expert, sized for a full expert; CTAs past an expert's count exit at once
+  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  int64_t bx = (cap * (K / 128) + per_block - 1) / per_block;
+  const int64_t limit = std::max<int64_t>(1, static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads) / E);
+  if (bx > limit) bx = limit;
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(E));
+  quantize_1x128_kernel<false, kE4M3, true><<<grid, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), K,
+      static_cast<uint8_t*>(q), K, sA, ld_sa, masked_m, static_cast<uint32_t>(cap));
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

@@ -196,3 +196,16 @@ def test_backward_entry_points_validation(lib):
     assert w(P, 256, P, 64, P, 256, P, 256, P, P + 2, 2, 64, 256, 256, None) == ALIGN
     assert w(P, 256, P, 66, P, 256, P, 256, P, P, 2, 64, 256, 256, None) == ALIGN     # ld_sa % 4
     assert w(P, 256, P, 64, P, 256, P, 256, P, P, 2, 0, 256, 256, None) == 0          # M == 0: no-op
+
+
+def test_masked_quantiser_validation(lib):
+    f = lib.fp8_quantize_1x128_masked
+    # (x, E, cap, K, masked_m, q, sA, ld_sa, stream)
+    assert f(P, 0, 256, 128, P, P, P, 256, None) == INVALID      # E
+    assert f(P, 2, 256, 100, P, P, P, 512, None) == INVALID      # K % 128
+    assert f(P, 2, 256, 128, P, P, P, 256, None) == INVALID      # ld_sa < E*cap
+    assert f(P, 2, 0, 128, None, None, None, 0, None) == 0        # cap == 0: no-op
+    assert f(P, 2, 256, 128, None, P, P, 512, None) == INVALID   # counts
+    assert f(P + 8, 2, 256, 128, P, P, P, 512, None) == ALIGN
+    assert f(P, 2, 256, 128, P + 2, P, P, 512, None) == ALIGN
+    assert f(P, 2, 256, 128, P, P, P, 514, None) == ALIGN        # ld_sa % 4

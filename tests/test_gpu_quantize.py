@@ -170,3 +170,32 @@ def test_1x128_every_amax_significand_against_every_x():
     xt = torch.from_numpy(np.stack(rows)).to(torch.bfloat16)
     assert torch.equal(xt.double(), torch.from_numpy(np.stack(rows)))  # every value is a bf16
     _check_1x128(xt)
+
+
+@pytest.mark.parametrize("E,cap,K", [(5, 256, 512), (3, 16, 128), (32, 256, 7168)])
+def test_masked_rows_quantiser(E, cap, K):
+    # only rows m < masked_m[e] are quantised (counts clamped to [0, cap]); the rest keep their bytes
+    import moe_grouped_gemm_block_gb300 as g
+    from oracle import quantize_1x128
+    gen = torch.Generator().manual_seed(E * cap + K)
+    x = (torch.randn((E, cap, K), generator=gen) * 2).to(torch.bfloat16)
+    counts = torch.randint(0, cap + 1, (E,), generator=gen, dtype=torch.int32)
+    counts[0] = 0
+    if E > 2:
+        counts[1] = cap
+        counts[2] = -3  # out of contract: clamped to 0
+    if E > 3:
+        counts[3] = cap + 7  # clamped to cap
+    q = torch.full((E, cap, K), 0xAB, dtype=torch.uint8, device="cuda")
+    ld = E * cap
+    sA = torch.full((K // 128, ld), -1.0, dtype=torch.float32, device="cuda")
+    g.fp8_quantize_1x128_masked(x.cuda(), q, sA, counts.cuda())
+    torch.cuda.synchronize()
+    qh, sh = q.cpu().numpy(), sA.cpu().numpy()
+    for e in range(E):
+        m = min(max(int(counts[e]), 0), cap)
+        if m:
+            q_ref, s_ref = quantize_1x128(x[e, :m].float().numpy())
+            assert np.array_equal(qh[e, :m], q_ref), e
+            assert np.array_equal(sh[:, e * cap:e * cap + m].T, s_ref), e
+        assert np.all(qh[e, m:] == 0xAB) and np.all(sh[:, e * cap + m:(e + 1) * cap] == -1.0), e
