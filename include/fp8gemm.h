@@ -7,6 +7,19 @@
  *     D[m, n] = bf16( sum_kb  P_kb[m, n] * sA[kb][m] * sB[n / 128][kb] )
  *     P_kb[m, n] = sum_{k in K block kb} A[m, k] * B[n, k]       (128-wide K blocks)
  *
+ * Calls (declared below in this order):
+ *   quantisation   fp8_quantize_1x128, fp8_quantize_1x128_masked, fp8_route_gather_quantize_1x128,
+ *                  fp8_quantize_128x128
+ *   GEMMs          fp8_gemm_nt, fp8_gemm_nt_noalloc, fp8_grouped_gemm_contiguous,
+ *                  fp8_grouped_gemm_masked
+ *   per-tensor / per-token / per-channel scales
+ *                  fp8_quantize_per_row, fp8_quantize_per_tensor, fp8_gemm_nt_scaled,
+ *                  fp8_grouped_gemm_contiguous_scaled, fp8_grouped_gemm_masked_scaled
+ *   backward (e5m2 gradients)
+ *                  fp8_quantize_1x128_e5m2, fp8_gemm_nt_dgrad, fp8_grouped_gemm_contiguous_dgrad,
+ *                  fp8_grouped_gemm_wgrad
+ *   status         fp8g_get_status, fp8g_status_string, fp8g_last_config
+ *
  * Sources (page title, section):
  *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
  *    scales for the activations A, per-channel scales for the weights B, K cut

@@ -28,6 +28,12 @@
 // place in one TMEM buffer (2 at BN = 256: the epilogue of one tile overlaps the MMAs of the
 // next), each K block's commit frees its stage, and the epilogue reads the accumulator once and
 // multiplies it by sa[m] * sb[n] before the BF16 store.
+// Backward forms (e5m2 gradients, "E4M3 vs E5M2" on the Production FP8 GEMM page): the operand
+// formats are a run-time field of the MMA instruction descriptor (A in e5m2 for the data
+// gradient), and the K-grouped mode computes one weight-gradient matrix per expert over that
+// expert's token range, with a B scale per column and K block applied in the promotion.
+// Stream-K tail: when the tiles do not fill whole rounds of the grid, the last round's K blocks
+// are split over all SMs and the partial sums are added by the CTA holding each tile's start.
 // Every wait is bounded: a wait that runs past its cycle budget records FP8G_ERR_TIMEOUT in
 // the status word, raises a shared abort flag, and every role returns.
 

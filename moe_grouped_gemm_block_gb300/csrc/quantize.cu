@@ -5,7 +5,12 @@
 // scale can be max_val / 448.  Activations get one scale per row and 128-wide K block,
 // weights one per 128x128 block (explainer sec. 5.1).
 //
-// Both kernels are HBM-bound (2 bytes read + 1 byte written per element): 16-byte
+// Also here: the 1x128 quantiser's gathering form (rows taken through a row -> token map, built
+// on the device from routed tokens by the layout kernels below), its masked-layout form (only each
+// expert's valid rows) and its e5m2 form for gradients (s = amax / 57344); per-row and per-tensor
+// scales (walk-through sec. 2.2).
+//
+// The quantisers are HBM-bound (2 bytes read + 1 byte written per element): 16-byte
 // coalesced loads, 8-byte coalesced stores, the e4m3 code of the IEEE fp32 quotient x / s
 // (a multiplication by 1/s, with the division kept for the rare elements where the two
 // could round differently) and the round-to-nearest-even saturating e4m3 conversion.
