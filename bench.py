@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import gc
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -242,14 +243,24 @@ class Case:
 KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "common.cuh"), "quant": ("quantize.cu", "ptx.cuh", "common.cuh")}
 
 
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/|\S+', re.S)
+
+
+def _code_only(text: str) -> str:
+    """C/C++ source without comments or layout: the tokens that reach the compiler, one space apart
+    (string literals kept whole, so a // inside one is not taken for a comment)."""
+    return " ".join(t for t in _CODE_TOKENS.findall(text) if not t.startswith(("//", "/*")))
+
+
 def source_digest(kind: str | None = None) -> str:
-    """Digest of csrc/ (kind None) or of the files one kernel kind is built from."""
+    """Digest of csrc/ (kind None) or of the files one kernel kind is built from, over their code
+    only: an edit of comments or layout leaves a kernel's recorded counters current."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_grouped_gemm_block_gb300", "csrc")
     names = sorted(os.listdir(csrc)) if kind is None else sorted(KERNEL_SOURCES[kind])
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

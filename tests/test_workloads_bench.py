@@ -110,3 +110,14 @@ def test_multi_rank_timing_takes_the_max_over_ranks():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=5) for _ in range(2))
     assert got == [(0, 2.5), (1, 2.5)]
+
+
+def test_source_digest_ignores_comments_and_layout_only():
+    import bench
+    a = 'int x = 1; // note\n/* block\n  comment */ const char* s = "a // b";\n'
+    b = 'int  x = 1;\n\n// another note\nconst char* s = "a // b"; /* more */\n'
+    c = 'int x = 2; const char* s = "a // b";'
+    d = 'int x = 1; const char* s = "a /* b";'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert bench._code_only(a) != bench._code_only(d)  # string contents are code
