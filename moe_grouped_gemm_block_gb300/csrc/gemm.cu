@@ -67,7 +67,11 @@ constexpr int kSAAhead = 4;  // K-block steps by which the A-row scales are load
 
 // PAIR: a cluster of two CTAs computes 256 x BN tiles with tcgen05.mma.cta_group::2; each CTA
 // loads its 128 A rows and half of the B tile (BN / 2 rows), so a stage is 32 KB and six fit.
-template <int BN, bool SMALL = false, bool PAIR = false>
+// KG: the K-grouped weight gradient, whose tiles are short (one expert's tokens): three stages
+// (its operands come mostly from L2) make room for a staging box per 32 columns in every store
+// warp, so a tile's boxes are stored without waiting on one another, and for each epilogue
+// warp's 512 bytes of per-column B scales.
+template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
 struct Cfg {
   static constexpr int kEpiCols = BN >= 128 ? 128 : BN;  // columns per epilogue warp
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
@@ -97,7 +101,8 @@ struct Cfg {
   // every row (a kKPS * 128-byte run in global memory): streaming weights from HBM in 128-byte
   // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
   static constexpr int kKPS = SMALL ? 2 : 1;
-  static constexpr int kStages = SMALL ? 6 : (PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6));
+  static constexpr int kStages =
+      SMALL ? 6 : (PAIR ? (BN == 256 ? 6 : 8) : (KG ? 3 : (BN == 256 ? 4 : 6)));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
@@ -107,14 +112,18 @@ struct Cfg {
   static constexpr uint32_t kBBytes = kBRows * BK;       // one K block of B
   static constexpr uint32_t kStageABytes = kKPS * kABytes;
   static constexpr uint32_t kStageBBytes = kKPS * kBBytes;
-  static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box per store warp
+  static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box
+  static constexpr int kOutBoxes = KG ? kEpiCols / 32 : 1;  // staging boxes per store warp
+  static constexpr uint32_t kOutWarpBytes = kOutBoxes * kOutBytes;
+  static constexpr uint32_t kSbvBytes = KG ? 512u * kEpiWarps : 0u;  // per-column B scales
   static constexpr int kXRows = SMALL ? 64 : BM;
   static constexpr uint32_t kXBytes = kKSplit > 1 ? kXRows * BN * 4 : 0;  // K-split exchange
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kStageABytes;
   static constexpr uint32_t kOffOut = kOffB + kStages * kStageBBytes;
-  static constexpr uint32_t kOffX = kOffOut + kStoreWarps * kOutBytes;
+  static constexpr uint32_t kOffSbv = kOffOut + kStoreWarps * kOutWarpBytes;
+  static constexpr uint32_t kOffX = kOffSbv + kSbvBytes;
   static constexpr uint32_t kOffBar = kOffX + kXBytes;
   static constexpr uint32_t kNumBars = 2 * kStages + 2 * kTmemBufs + 4;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
@@ -415,11 +424,11 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* f, const GemmArgs& a, 
 }
 
 template <int BN, int MODE, bool PAIR = false, bool EPI = false>
-__global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD,
                     const GemmArgs a) {
-  using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
+  using C = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>;
   static_assert(!EPI || (C::kKSplit == 1 && C::kMmaWarps == 1 && !PAIR),
                 "epilogue scaling: one K part, one issuer, single-CTA tiles");
   static_assert(MODE != kKGrouped || (!EPI && !PAIR && C::kMmaWarps == 1),
@@ -788,7 +797,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         else mbar_arrive(tempty(b));
       }
     };
-    const uint32_t out_addr = base + C::kOffOut + (ew % C::kStoreWarps) * C::kOutBytes;
+    const uint32_t out_addr = base + C::kOffOut + (ew % C::kStoreWarps) * C::kOutWarpBytes;
+    const uint32_t sbv_addr = base + C::kOffSbv + ew * 512u;  // K-grouped: this warp's B scales
     float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
     uint32_t it_base = 0, tiles_done = 0;
     uint32_t np = 0;  // pieces taken (EPI: the TMEM buffer sequence, as the MMA warp counts it)
@@ -849,13 +859,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
         // K-grouped: the B scales of this warp's columns for one K block, lane l loading columns
-        // 4l .. 4l+3 (one coalesced 16-byte load per lane, a K block ahead).  They are staged in
-        // the first 512 bytes of this warp's output box (idle until the tile's store; the previous
-        // tile's store must have finished reading it) and read back with warp-uniform addresses.
-        if (MODE == kKGrouped) {
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-        }
+        // 4l .. 4l+3 (one coalesced 16-byte load per lane, a K block ahead), staged in this warp's
+        // 512 bytes of shared memory and read back with warp-uniform addresses.
         auto load_sbv = [&](int32_t kbi) {
           float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
           if (MODE == kKGrouped && kbi < pc.kb1 && ncol0 + 4 * lane < a.N)
@@ -867,7 +872,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
         for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += C::kKSplit) {
           if (MODE == kKGrouped) {
             __syncwarp();  // every lane has read the previous K block's scales
-            st_shared_v4(out_addr + 16 * lane, __float_as_uint(sbv_nxt.x), __float_as_uint(sbv_nxt.y),
+            st_shared_v4(sbv_addr + 16 * lane, __float_as_uint(sbv_nxt.x), __float_as_uint(sbv_nxt.y),
                          __float_as_uint(sbv_nxt.z), __float_as_uint(sbv_nxt.w));
             __syncwarp();
           }
@@ -909,7 +914,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
                 const float2 sa2 = make_float2(sa_kb, sa_kb);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                  const float4 s4 = ld_shared_v4f(out_addr + 16 * (c * 16 + i));
+                  const float4 s4 = ld_shared_v4f(sbv_addr + 16 * (c * 16 + i));
                   const float2 s01 = __fmul2_rn(sa2, make_float2(s4.x, s4.y));
                   const float2 s23 = __fmul2_rn(sa2, make_float2(s4.z, s4.w));
                   acc[c * 32 + 2 * i] = __ffma2_rn(make_float2(v[4 * i], v[4 * i + 1]), s01, acc[c * 32 + 2 * i]);
@@ -1019,12 +1024,17 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 32; ++j) {
           if (ncol0 + 32 * j >= a.N) break;
-          if (lane == 0) bulk_wait_read_all();  // the previous box has left the buffer
-          __syncwarp();
+          // the staging box has left for global memory: with one box per warp, the previous box;
+          // with a box per 32 columns (K-grouped), the previous tile's boxes
+          const uint32_t box = out_addr + (C::kOutBoxes > 1 ? j * C::kOutBytes : 0u);
+          if (C::kOutBoxes == 1 || j == 0) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
           uint32_t p[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(acc[16 * j + i].x, acc[16 * j + i].y);
-          const uint32_t rowaddr = out_addr + lane * 64;
+          const uint32_t rowaddr = box + lane * 64;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             // 64-byte swizzle: 16-byte chunk index XOR address bits 7-8 (= row / 2 mod 4)
@@ -1034,7 +1044,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmD, out_addr, ncol0 + 32 * j, ti.d_row + q * 32);
+            tma_store_2d(&tmD, box, ncol0 + 32 * j, ti.d_row + q * 32);
             bulk_commit();
           }
         }
@@ -1070,9 +1080,9 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR>::kThreads,
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool SMALL = false, bool PAIR = false>
+template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
 constexpr uint32_t smem_bytes(int table_entries) {
-  return Cfg<BN, SMALL, PAIR>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
+  return Cfg<BN, SMALL, PAIR, KG>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
 }
 
 constexpr int kMaxExperts = 2048;
@@ -1083,12 +1093,14 @@ static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<256, false, false, true>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<128, false, false, true>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 
 template <int BN, int MODE, bool PAIR = false, bool EPI = false>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
                   const CUtensorMap& tD, int grid, int table_entries,
                   cudaStream_t stream) {
-  using C = Cfg<BN, MODE == kDenseSmallM, PAIR>;
+  using C = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>;
   auto kern = fp8_gemm_kernel<BN, MODE, PAIR, EPI>;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
   int dev = 0;
@@ -1114,7 +1126,7 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     }
     attr_set.fetch_or(bit);
   }
-  const uint32_t smem = smem_bytes<BN, MODE == kDenseSmallM, PAIR>(table_entries);
+  const uint32_t smem = smem_bytes<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>(table_entries);
   if constexpr (PAIR) {  // clusters of two CTAs (the grid is even)
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1412,10 +1424,10 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   t_last_grid = grid;
   if constexpr (MODE == kKGrouped) {
     if (bn == 256) {
-      t_last_stages = Cfg<256>::kStages;
+      t_last_stages = Cfg<256, false, false, true>::kStages;
       return launch_kernel<256, kKGrouped>(a, tA, tB, tD, grid, table_entries, stream);
     }
-    t_last_stages = Cfg<128>::kStages;
+    t_last_stages = Cfg<128, false, false, true>::kStages;
     return launch_kernel<128, kKGrouped>(a, tA, tB, tD, grid, table_entries, stream);
   } else if constexpr (EPI) {
     if (bn == 256) {
