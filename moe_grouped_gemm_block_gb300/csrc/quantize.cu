@@ -81,28 +81,35 @@ __device__ __forceinline__ uint32_t cvt_x4(float a0, float a1, float a2, float a
   return FMT == kE5M2 ? cvt_e5m2x4(a0, a1, a2, a3) : cvt_e4m3x4(a0, a1, a2, a3);
 }
 
-// Direct path.  For most blocks the single product y = RN(x * RN(1/s)) already has the code of
-// RN(x / s) for every bf16 x with |x| <= amax, and no bracket is needed.  Whether it does depends
-// only on amax's 8-bit bf16 significand A (with s normal, s, 1/s, the products and the codes all
-// scale exactly with a power-of-two change of amax and x), so an exhaustive enumeration over A and
-// every x settles it: bit (A - 128) of the kDirectSafe words is set when no x gives a different code (102 of
-// the 128 significands).  gen_quant_tables.py, next to this package, produces the table.
-constexpr uint32_t kDirectSafe0 = 0xFCFFFBEFu, kDirectSafe1 = 0x7EB9BB37u,  // A = 128..159, 160..191
-                   kDirectSafe2 = 0xFFDACFA7u, kDirectSafe3 = 0xF2FFF7FFu;  // A = 192..223, 224..255
+// Direct path.  For most blocks a single product y = RN(x * r) with a fixed multiplier r already
+// has the code of RN(x / s) for every bf16 x with |x| <= amax, and no bracket is needed.  Whether a
+// given r works depends only on amax's 8-bit bf16 significand A (with s normal, s, 1/s, the
+// products and the codes all scale exactly with a power-of-two change of amax and x, and so does r
+// moved by whole ulps), so an exhaustive enumeration over A and every x settles it.  The kDirectMode
+// words hold 2 bits per A (bits 2 (i % 16) of word i / 16, i = A - 128): 1 = r is RN(1/s) (102 of
+// the 128 significands), 2 = RN(1/s) one ulp up (15), 3 = one ulp down (4), 0 = no single multiplier
+// works (7): keep the bracket.  gen_quant_tables.py, next to this package, produces the table.
+constexpr uint32_t kDirectMode0 = 0x55755655u, kDirectMode1 = 0x555B5555u,  // A = 128..143, 144..159
+                   kDirectMode2 = 0x656585D5u, kDirectMode3 = 0x95544569u,  // A = 160..175, 176..191
+                   kDirectMode4 = 0x58556495u, kDirectMode5 = 0x55555944u,  // A = 192..207, 208..223
+                   kDirectMode6 = 0x55D55555u, kDirectMode7 = 0x55A65555u;  // A = 224..239, 240..255
 
-// True when the block's codes can be taken from the direct product (amax as a float holding a
-// bf16 value; s its scale).
-__device__ __forceinline__ bool direct_ok(float amax, float s) {
+// The block's direct-path mode (amax as a float holding a bf16 value; s its scale): 0 when the
+// bracket is needed (or s is not normal).
+__device__ __forceinline__ uint32_t direct_mode(float amax, float s) {
   const uint32_t a7 = (__float_as_uint(amax) >> 16) & 0x7Fu;  // amax's stored mantissa bits
-  const uint32_t word = a7 < 64u ? (a7 < 32u ? kDirectSafe0 : kDirectSafe1)
-                                 : (a7 < 96u ? kDirectSafe2 : kDirectSafe3);
-  return s >= 1.17549435e-38f && ((word >> (a7 & 31u)) & 1u) != 0u;
+  const uint32_t g = a7 >> 4;
+  const uint32_t word = g < 4u ? (g < 2u ? (g == 0u ? kDirectMode0 : kDirectMode1)
+                                         : (g == 2u ? kDirectMode2 : kDirectMode3))
+                               : (g < 6u ? (g == 4u ? kDirectMode4 : kDirectMode5)
+                                         : (g == 6u ? kDirectMode6 : kDirectMode7));
+  return s >= 1.17549435e-38f ? (word >> (2u * (a7 & 15u))) & 3u : 0u;
 }
 
 // FMT e5m2: the bracket argument holds for any monotone round-to-nearest conversion; the direct
-// path's table is e4m3's, so e5m2 callers pass direct = false.
+// path's table is e4m3's, so e5m2 callers pass mode 0.
 template <int N, int FMT = kE4M3>
-__device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direct, uint32_t (&w)[N / 4]) {
+__device__ __forceinline__ void quant_n(const float (&f)[N], float s, uint32_t direct, uint32_t (&w)[N / 4]) {
   static_assert(N % 4 == 0, "N");
   if (s == 0.0f) {
 #pragma unroll
@@ -111,7 +118,8 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direc
   }
   bool exact = !(s >= 1.17549435e-38f);  // subnormal s: divide every element
   if (!exact && direct) {
-    const float r = __frcp_rn(s);
+    // RN(1/s), moved one ulp up (mode 2) or down (mode 3); r is a normal float here
+    const float r = __uint_as_float(__float_as_uint(__frcp_rn(s)) + (direct == 2u) - (direct == 3u));
     const float2 r2 = make_float2(r, r);
 #pragma unroll
     for (int i = 0; i < N / 4; ++i) {
@@ -144,7 +152,7 @@ __device__ __forceinline__ void quant_n(const float (&f)[N], float s, bool direc
   }
 }
 
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, bool direct) {
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, uint32_t direct) {
   uint32_t w[2];
   quant_n<8>(f, s, direct, w);
   return make_uint2(w[0], w[1]);
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
       const float s = __fdiv_rn(a, FMT == kE5M2 ? kE5M2Max : kE4M3Max);
       if (live[u]) {
         uint32_t c[4];
-        quant_n<16, FMT>(f, s, FMT == kE4M3 && direct_ok(a, s), c);
+        quant_n<16, FMT>(f, s, FMT == kE4M3 ? direct_mode(a, s) : 0u, c);
         uint8_t* dst = q + m[u] * ldq + kb[u] * 128 + sub * 8;
         *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
         *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(256) quantize_128x128_kernel(
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   const float s = __fdiv_rn(amax, kE4M3Max);
-  const bool direct = direct_ok(amax, s);
+  const uint32_t direct = direct_mode(amax, s);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = r0 + 16 * i;
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(
   }
   const float amax = block_amax(a, red);
   const float s = __fdiv_rn(amax, kE4M3Max);
-  const bool direct = direct_ok(amax, s);
+  const uint32_t direct = direct_mode(amax, s);
 #pragma unroll
   for (int i = 0; i < kRowVec; ++i) {
     const int64_t v = t + static_cast<int64_t>(i) * kRowThreads;
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kTensorThreads) quantize_tensor_kernel(
   const uint32_t e = blockIdx.y;
   const float s = __ldg(s_in + e);
   const float amax = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s, kE4M3Max)));
-  const bool direct = direct_ok(amax, s);
+  const uint32_t direct = direct_mode(amax, s);
   const uint32_t total = M * kvec;
   for (uint32_t p = blockIdx.x * kTensorThreads + threadIdx.x; p < total; p += gridDim.x * kTensorThreads) {
     const uint32_t r = p / kvec, v = p - r * kvec;
