@@ -18,7 +18,7 @@
  *   backward (e5m2 gradients)
  *                  fp8_quantize_1x128_e5m2, fp8_gemm_nt_dgrad, fp8_grouped_gemm_contiguous_dgrad,
  *                  fp8_grouped_gemm_wgrad
- *   status         fp8g_get_status, fp8g_status_string, fp8g_last_config
+ *   status         fp8g_get_status, fp8g_status_string, fp8g_selftest_bounded_waits, fp8g_last_config
  *
  * Sources (page title, section):
  *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
@@ -387,6 +387,16 @@ int fp8g_get_status(void* stream);
 
 /* fp8g_status_string -- a static, human-readable name for a status code. */
 const char* fp8g_status_string(int code);
+
+/*
+ * fp8g_selftest_bounded_waits -- runs, on `stream`, the bounded waits every GEMM role uses against
+ * an mbarrier phase that nothing completes and a flag that nothing raises (one thread, nothing in
+ * flight), each with a budget of `budget_cycles` clock cycles.  Both must run out: out[0] and out[1]
+ * are set to 1 when the mbarrier and the flag wait gave up, out[2] to 1 when both raised the abort
+ * flag, and the status word records FP8G_ERR_TIMEOUT (read it with fp8g_get_status).  The CUDA
+ * context stays usable.  out: uint32 [3], device memory.  0 < budget_cycles <= 2^40.
+ */
+int fp8g_selftest_bounded_waits(int64_t budget_cycles, uint32_t* out, void* stream);
 
 /*
  * fp8g_last_config -- the tile configuration the last GEMM call on this thread

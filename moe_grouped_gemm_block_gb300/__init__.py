@@ -73,6 +73,7 @@ _SIGNATURES = {
     "fp8_gemm_nt_dgrad": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_contiguous_dgrad": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_wgrad": [_P, _I64, _FP, _I64, _P, _I64, _FP, _I64, _P, _P, _I32, _I64, _I64, _I64, _P],
+    "fp8g_selftest_bounded_waits": [_I64, _P, _P],
     "fp8g_get_status": [_P],
     "fp8g_last_config": [ctypes.POINTER(ctypes.c_int)] * 3,
 }

@@ -1078,6 +1078,29 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
   }
 }
 
+// Self-test of the bounded waits the GEMM's roles use: one thread waits on an mbarrier phase that
+// nothing completes, then on a global flag that nothing raises.  Nothing is in flight, so each wait
+// can only run out of its budget; each must then record FP8G_ERR_TIMEOUT and return false.
+// out[0] / out[1]: 1 when the mbarrier / flag wait returned false, out[2]: the abort flag.
+__device__ uint32_t g_never_raised = 0u;
+
+__global__ void bounded_wait_selftest_kernel(const GemmArgs a, uint32_t* out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  volatile int* abort_flag = &abort_word;
+  *abort_flag = 0;
+  const bool bar_ok = wait_bounded(smem_u32(&bar), 0u, a, abort_flag);  // phase 0: no arrival
+  const int abort_after_bar = *abort_flag;
+  *abort_flag = 0;
+  const bool flag_ok = wait_flag(&g_never_raised, a, abort_flag);
+  out[0] = bar_ok ? 0u : 1u;
+  out[1] = flag_ok ? 0u : 1u;
+  out[2] = static_cast<uint32_t>(abort_after_bar && *abort_flag);
+}
+
 // ---------------------------------------------------------------- host side
 
 template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
@@ -1669,6 +1692,19 @@ extern "C" int fp8_grouped_gemm_masked_scaled(const void* A, const float* sA, in
   Operands o{A, K, sA, 0, B, K, sB, D, N, static_cast<int64_t>(E) * cap, N, K, E, cap, masked_m,
              sa_per_row, sb_per_col};
   return run_gemm<kMasked, true>(o, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8g_selftest_bounded_waits(int64_t budget_cycles, uint32_t* out, void* stream) {
+  if (budget_cycles <= 0 || budget_cycles > (int64_t{1} << 40) || !out) return FP8G_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 3u) return FP8G_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  const int st = current_device(&dev);
+  if (st != FP8G_OK) return st;
+  GemmArgs a{};
+  a.status = dev->status;
+  a.budget = budget_cycles;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(a, out);
+  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
 extern "C" int fp8g_last_config(int* block_n, int* stages, int* grid) {

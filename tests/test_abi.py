@@ -209,3 +209,12 @@ def test_masked_quantiser_validation(lib):
     assert f(P + 8, 2, 256, 128, P, P, P, 512, None) == ALIGN
     assert f(P, 2, 256, 128, P + 2, P, P, 512, None) == ALIGN
     assert f(P, 2, 256, 128, P, P, P, 514, None) == ALIGN        # ld_sa % 4
+
+
+def test_selftest_validation(lib):
+    f = lib.fp8g_selftest_bounded_waits
+    assert f(0, P, None) == INVALID
+    assert f(-5, P, None) == INVALID
+    assert f(1 << 41, P, None) == INVALID
+    assert f(1000, None, None) == INVALID
+    assert f(1000, P + 2, None) == ALIGN
