@@ -52,7 +52,8 @@ class Workload:
     extra: dict = field(default_factory=dict, compare=False)
 
 
-# The five configurations of the benchmark spec, plus the second large shape.
+# The workloads: a tiny dense case, a decode shape, two large dense shapes (4096^3 and the
+# 4096 x 8192 x 8192 shape of the H100 table), and the two MoE layouts.
 WORKLOADS = {
     "tiny": Workload("tiny", "dense", M=128, N=256, K=512, seed=0, b_std_one=True),
     "decode": Workload("decode", "dense", M=64, N=7168, K=7168, seed=1, outliers=True),
