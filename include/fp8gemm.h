@@ -48,7 +48,8 @@
  *    fp8g_get_status reads and clears; the kernel returns early instead of
  *    trapping, so the CUDA context stays usable.
  *  - e4m3 bytes use the OCP "e4m3fn" encoding (no infinities, 0x7F/0xFF NaN,
- *    max 448).  Inputs must be finite.
+ *    max 448); e5m2 bytes (gradients) the OCP "E5M2" encoding (max 57344, with
+ *    infinities and NaN in the top exponent).  Inputs must be finite.
  *  - Only sm_103 devices are supported; anything else returns
  *    FP8G_ERR_UNSUPPORTED_DEVICE (there is no fallback path).
  *  - Calls are thread-safe; calls on different streams may run concurrently.
