@@ -800,10 +800,19 @@ def cpu_baseline(names, target_s=15.0):
             "seconds": round(tot_t, 2)}
 
 
-def run_reference(args, world, rank):
+def run_reference(args, world, rank, budget_s=120.0):
     if rank != 0:
         return
     samples = oracle_sample(args.workloads)
+    # one step decides the sample size: the whole run stays within about budget_s on these cores
+    _, t1 = time_oracle(samples)
+    projected = t1 * (args.steps + args.warmup)
+    scale = 1.0
+    if projected > budget_s:
+        scale = max(0.125, 0.75 * budget_s / projected)
+        samples = oracle_sample(args.workloads, scale)
+    rows = max(8, int(64 * scale))
+    cols = 128 * max(1, int(8 * scale))
     for _ in range(args.warmup):
         time_oracle(samples)
     tot_f, tot_t = 0.0, 0.0
@@ -818,7 +827,7 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 block dots, f32 promotion",
         "data": "synthetic", "config": {"workload": "+".join(args.workloads), "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": "each step: 64 rows x 1024 weight rows of every workload"},
+                         "sample": f"each step: {rows} rows x {cols} weight rows of every workload"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)

@@ -121,3 +121,22 @@ def test_source_digest_ignores_comments_and_layout_only():
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
     assert bench._code_only(a) != bench._code_only(d)  # string contents are code
+
+
+def test_reference_arm_prints_the_contract_line():
+    # `bench.py --impl reference` times the oracle on the host cores; its line carries the contract's
+    # keys, the reference marker, and describes the sample it timed
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "1", "--workloads", "tiny,decode"], capture_output=True, text=True, cwd=root,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    for key in ("metric", "unit", "n_gpus", "ms_per_step", "higher_is_better", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["cpu_baseline"]["kind"] == "oracle" and "rows" in line["cpu_baseline"]["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
