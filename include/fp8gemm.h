@@ -18,7 +18,8 @@
  *   backward (e5m2 gradients)
  *                  fp8_quantize_1x128_e5m2, fp8_gemm_nt_dgrad, fp8_grouped_gemm_contiguous_dgrad,
  *                  fp8_grouped_gemm_wgrad
- *   status         fp8g_get_status, fp8g_status_string, fp8g_selftest_bounded_waits, fp8g_last_config
+ *   status         fp8g_get_status, fp8g_status_string, fp8g_selftest_bounded_waits, fp8g_last_config,
+ *                  fp8g_last_split
  *
  * Sources (page title, section):
  *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
@@ -187,9 +188,11 @@ int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa, cons
  * pool expects every device buffer to come from it.  fp8_gemm_nt allocates its
  * workspace on the first call on each stream that splits tiles; this call uses a
  * fixed buffer that is part of the library's device image instead: 160 stream-K
- * slots of 128 KiB plus 1 KiB of flags (20 MiB + 1 KiB, present once the library's
- * kernels are loaded).  It does clear the flags with a memset on `stream` before
- * each launch.
+ * slots of 128 KiB plus 1 KiB of flags (20 MiB + 1 KiB).  The buffer sits in a module
+ * of its own: under lazy module loading (the CUDA default) a device holds it only
+ * once this call has run there, until the process exits; with eager loading every
+ * device that loads the library holds it.  It does clear the flags with a memset on
+ * `stream` before each launch.
  *
  * Same arguments, results and errors as fp8_gemm_nt, plus:
  *  - a device with more than 160 SMs is out of the buffer's range and gets
@@ -200,7 +203,8 @@ int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa, cons
  *    caller must order them (one stream, or events);
  *  - the first call on each device looks up the buffer's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call before
- *    capturing any stream.
+ *    capturing any stream.  A lookup that fails returns FP8G_ERR_CUDA and is tried
+ *    again on the next call.
  */
 int fp8_gemm_nt_noalloc(const void* A, int64_t lda, const float* sA, int64_t ld_sa, const void* B,
                         int64_t ldb, const float* sB, void* D, int64_t ldd, int64_t M, int64_t N,
@@ -405,6 +409,15 @@ int fp8g_selftest_bounded_waits(int64_t budget_cycles, uint32_t* out, void* stre
  * Diagnostic only; returns FP8G_OK, or FP8G_ERR_INVALID_ARG for null pointers.
  */
 int fp8g_last_config(int* block_n, int* stages, int* grid);
+
+/*
+ * fp8g_last_split -- 1 when the last GEMM call on this thread split the K blocks of its
+ * last round of tiles over every SM (the stream-K tail, which uses the GEMM workspace or,
+ * for fp8_gemm_nt_noalloc, the fixed scratch), else 0.  The masked form decides on the
+ * device: 1 there means the launch could split.  Diagnostic only; returns FP8G_OK, or
+ * FP8G_ERR_INVALID_ARG for a null pointer.
+ */
+int fp8g_last_split(int* split);
 
 #ifdef __cplusplus
 }

@@ -76,6 +76,7 @@ _SIGNATURES = {
     "fp8g_selftest_bounded_waits": [_I64, _P, _P],
     "fp8g_get_status": [_P],
     "fp8g_last_config": [ctypes.POINTER(ctypes.c_int)] * 3,
+    "fp8g_last_split": [ctypes.POINTER(ctypes.c_int)],
 }
 
 
@@ -130,6 +131,25 @@ def _need(cond: bool, msg: str):
         raise ValueError(msg)
 
 
+def _block_scales(sA: torch.Tensor, sB: torch.Tensor, rows: int, N: int, K: int, E: int) -> int:
+    """Checks the 1x128 activation scales sA [K/128, ld_sa >= rows] (row stride ld_sa, unit column
+    stride) and the 128x128 weight scales sB [E, ceil(N/128), K/128] (contiguous) against the
+    problem size, so that no kernel reads past either; returns ld_sa."""
+    _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1
+          and sA.shape[1] >= rows and (sA.shape[0] == 1 or sA.stride(0) >= sA.shape[1]),
+          f"sA: f32 [K/128, ld_sa >= {rows}]")
+    _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() == E * ((N + 127) // 128) * (K // 128),
+          f"sB: f32 [{E}, ceil(N/128), K/128] contiguous")
+    return sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+
+
+def _on_one_device(*ts: torch.Tensor):
+    """Every operand, group offsets and counts included, in device memory of one GPU: the library
+    dereferences them all on the device (the host never reads the offsets or counts)."""
+    dev = ts[0].device
+    _need(all(t.is_cuda and t.device == dev for t in ts), "operands: CUDA tensors on one device")
+
+
 # ------------------------------------------------------------------ C-ABI calls
 
 def fp8_quantize_1x128(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor) -> None:
@@ -139,6 +159,8 @@ def fp8_quantize_1x128(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor) -> No
     _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1,
           "sA: f32 [K/128, ld_sa]")
     ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(sA.shape[1] >= M, "sA: f32 [K/128, ld_sa >= M]")
+    _on_one_device(x, q, sA)
     _check(lib().fp8_quantize_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(sA), ld_sa,
                                     _stream(x)), "fp8_quantize_1x128")
 
@@ -149,6 +171,7 @@ def fp8_quantize_128x128(w: torch.Tensor, q: torch.Tensor, sB: torch.Tensor) -> 
     E, N, K = (1, *w.shape) if w.dim() == 2 else w.shape
     _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() == E * ((N + 127) // 128) * (K // 128),
           "sB: f32 [E, ceil(N/128), K/128] contiguous")
+    _on_one_device(w, q, sB)
     _check(lib().fp8_quantize_128x128(_ptr(w), E, N, K, _ptr(q), _ptr(sB), _stream(w)),
            "fp8_quantize_128x128")
 
@@ -157,10 +180,11 @@ def fp8_gemm_nt(A, sA, B, sB, D) -> None:
     _need(_is_fp8(A) and A.dim() == 2 and A.stride(1) == 1, "A: e4m3 [M,K]")
     _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
     _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
-    _need(sA.dtype == torch.float32 and sB.dtype == torch.float32 and sB.is_contiguous(), "scales: f32")
     M, K = A.shape
     N = B.shape[0]
-    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(B.shape[1] == K and D.shape == (M, N), "shapes: A [M,K], B [N,K], D [M,N]")
+    ld_sa = _block_scales(sA, sB, M, N, K, 1)
+    _on_one_device(A, sA, B, sB, D)
     _check(lib().fp8_gemm_nt(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
                              _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt")
 
@@ -172,10 +196,11 @@ def fp8_gemm_nt_noalloc(A, sA, B, sB, D) -> None:
     _need(_is_fp8(A) and A.dim() == 2 and A.stride(1) == 1, "A: e4m3 [M,K]")
     _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
     _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
-    _need(sA.dtype == torch.float32 and sB.dtype == torch.float32 and sB.is_contiguous(), "scales: f32")
     M, K = A.shape
     N = B.shape[0]
-    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(B.shape[1] == K and D.shape == (M, N), "shapes: A [M,K], B [N,K], D [M,N]")
+    ld_sa = _block_scales(sA, sB, M, N, K, 1)
+    _on_one_device(A, sA, B, sB, D)
     _check(lib().fp8_gemm_nt_noalloc(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
                                      _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt_noalloc")
 
@@ -184,10 +209,13 @@ def fp8_grouped_gemm_contiguous(A, sA, B, sB, D, group_offsets) -> None:
     _need(_is_fp8(A) and A.dim() == 2 and A.is_contiguous(), "A: e4m3 [M_total,K] contiguous")
     _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
     _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [M_total,N] contiguous")
-    _need(group_offsets.dtype == torch.int32 and group_offsets.is_cuda, "group_offsets: int32 device tensor")
+    _need(group_offsets.dtype == torch.int32, "group_offsets: int32 device tensor")
     M_total, K = A.shape
     E, N, _ = B.shape
-    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(B.shape[2] == K and D.shape == (M_total, N) and group_offsets.numel() == E + 1,
+          "shapes: A [M_total,K], B [E,N,K], D [M_total,N], group_offsets [E+1]")
+    ld_sa = _block_scales(sA, sB, M_total, N, K, E)
+    _on_one_device(A, sA, B, sB, D, group_offsets)
     _check(lib().fp8_grouped_gemm_contiguous(_ptr(A), _ptr(sA), ld_sa, _ptr(B), _ptr(sB), _ptr(D),
                                              _ptr(group_offsets), E, M_total, N, K, _stream(A)),
            "fp8_grouped_gemm_contiguous")
@@ -197,10 +225,13 @@ def fp8_grouped_gemm_masked(A, sA, B, sB, D, masked_m) -> None:
     _need(_is_fp8(A) and A.dim() == 3 and A.is_contiguous(), "A: e4m3 [E,cap,K] contiguous")
     _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
     _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [E,cap,N] contiguous")
-    _need(masked_m.dtype == torch.int32 and masked_m.is_cuda, "masked_m: int32 device tensor")
+    _need(masked_m.dtype == torch.int32, "masked_m: int32 device tensor")
     E, cap, K = A.shape
     N = B.shape[1]
-    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(B.shape[0] == E and B.shape[2] == K and D.shape == (E, cap, N) and masked_m.numel() == E,
+          "shapes: A [E,cap,K], B [E,N,K], D [E,cap,N], masked_m [E]")
+    ld_sa = _block_scales(sA, sB, E * cap, N, K, E)
+    _on_one_device(A, sA, B, sB, D, masked_m)
     _check(lib().fp8_grouped_gemm_masked(_ptr(A), _ptr(sA), ld_sa, _ptr(B), _ptr(sB), _ptr(D),
                                          _ptr(masked_m), E, cap, N, K, _stream(A)),
            "fp8_grouped_gemm_masked")
@@ -211,6 +242,7 @@ def fp8_quantize_per_row(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor) -> N
     _need(_is_fp8(q) and q.shape == x.shape and q.stride(1) == 1, "q: e4m3 [M,K]")
     M, K = x.shape
     _need(s.dtype == torch.float32 and s.is_contiguous() and s.numel() == M, "s: f32 [M]")
+    _on_one_device(x, q, s)
     _check(lib().fp8_quantize_per_row(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream(x)),
            "fp8_quantize_per_row")
 
@@ -221,6 +253,7 @@ def fp8_quantize_per_tensor(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor) -
     _need(_is_fp8(q) and q.shape == x.shape and q.is_contiguous(), "q: e4m3, same shape as x")
     E, M, K = (1, *x.shape) if x.dim() == 2 else x.shape
     _need(s.dtype == torch.float32 and s.is_contiguous() and s.numel() == E, "s: f32 [E]")
+    _on_one_device(x, q, s)
     _check(lib().fp8_quantize_per_tensor(_ptr(x), E, M, K, K, _ptr(q), K, _ptr(s), _stream(x)),
            "fp8_quantize_per_tensor")
 
@@ -237,7 +270,9 @@ def fp8_gemm_nt_scaled(A, sA, B, sB, D) -> None:
     _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
     M, K = A.shape
     N = B.shape[0]
+    _need(B.shape[1] == K and D.shape == (M, N), "shapes: A [M,K], B [N,K], D [M,N]")
     pa, pb = _epi_scale(sA, M, "sA"), _epi_scale(sB, N, "sB")
+    _on_one_device(A, sA, B, sB, D)
     _check(lib().fp8_gemm_nt_scaled(_ptr(A), A.stride(0), _ptr(sA), pa, _ptr(B), B.stride(0), _ptr(sB), pb,
                                     _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt_scaled")
 
@@ -246,12 +281,15 @@ def fp8_grouped_gemm_contiguous_scaled(A, sA, B, sB, D, group_offsets) -> None:
     _need(_is_fp8(A) and A.dim() == 2 and A.is_contiguous(), "A: e4m3 [M_total,K] contiguous")
     _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
     _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [M_total,N] contiguous")
-    _need(group_offsets.dtype == torch.int32 and group_offsets.is_cuda, "group_offsets: int32 device tensor")
+    _need(group_offsets.dtype == torch.int32, "group_offsets: int32 device tensor")
     M_total, K = A.shape
     E, N, _ = B.shape
     pa = _epi_scale(sA, M_total, "sA")
     _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() in (E, E * N), "sB: f32 [E,N] or [E]")
     pb = 1 if sB.numel() == E * N and N != 1 else 0
+    _need(B.shape[2] == K and D.shape == (M_total, N) and group_offsets.numel() == E + 1,
+          "shapes: A [M_total,K], B [E,N,K], D [M_total,N], group_offsets [E+1]")
+    _on_one_device(A, sA, B, sB, D, group_offsets)
     _check(lib().fp8_grouped_gemm_contiguous_scaled(_ptr(A), _ptr(sA), pa, _ptr(B), _ptr(sB), pb, _ptr(D),
                                                     _ptr(group_offsets), E, M_total, N, K, _stream(A)),
            "fp8_grouped_gemm_contiguous_scaled")
@@ -261,12 +299,15 @@ def fp8_grouped_gemm_masked_scaled(A, sA, B, sB, D, masked_m) -> None:
     _need(_is_fp8(A) and A.dim() == 3 and A.is_contiguous(), "A: e4m3 [E,cap,K] contiguous")
     _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
     _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [E,cap,N] contiguous")
-    _need(masked_m.dtype == torch.int32 and masked_m.is_cuda, "masked_m: int32 device tensor")
+    _need(masked_m.dtype == torch.int32, "masked_m: int32 device tensor")
     E, cap, K = A.shape
     N = B.shape[1]
     pa = _epi_scale(sA, E * cap, "sA")
     _need(sB.dtype == torch.float32 and sB.is_contiguous() and sB.numel() in (E, E * N), "sB: f32 [E,N] or [E]")
     pb = 1 if sB.numel() == E * N and N != 1 else 0
+    _need(B.shape[0] == E and B.shape[2] == K and D.shape == (E, cap, N) and masked_m.numel() == E,
+          "shapes: A [E,cap,K], B [E,N,K], D [E,cap,N], masked_m [E]")
+    _on_one_device(A, sA, B, sB, D, masked_m)
     _check(lib().fp8_grouped_gemm_masked_scaled(_ptr(A), _ptr(sA), pa, _ptr(B), _ptr(sB), pb, _ptr(D),
                                                 _ptr(masked_m), E, cap, N, K, _stream(A)),
            "fp8_grouped_gemm_masked_scaled")
@@ -276,11 +317,13 @@ def fp8_quantize_1x128_masked(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor
     """x bf16 [E,cap,K] -> q e4m3 [E,cap,K], sA f32 [K/128, ld_sa >= E*cap]: only rows m < masked_m[e]."""
     _need(x.dtype == torch.bfloat16 and x.dim() == 3 and x.is_contiguous(), "x: bf16 [E,cap,K] contiguous")
     _need(_is_fp8(q) and q.shape == x.shape and q.is_contiguous(), "q: e4m3 [E,cap,K] contiguous")
-    _need(masked_m.dtype == torch.int32 and masked_m.is_cuda, "masked_m: int32 device tensor")
+    _need(masked_m.dtype == torch.int32, "masked_m: int32 device tensor")
     E, cap, K = x.shape
     _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1,
           "sA: f32 [K/128, ld_sa]")
     ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(sA.shape[1] >= E * cap and masked_m.numel() == E, "sA: f32 [K/128, ld_sa >= E*cap]; masked_m [E]")
+    _on_one_device(x, q, sA, masked_m)
     _check(lib().fp8_quantize_1x128_masked(_ptr(x), E, cap, K, _ptr(masked_m), _ptr(q), _ptr(sA), ld_sa,
                                            _stream(x)), "fp8_quantize_1x128_masked")
 
@@ -292,6 +335,8 @@ def fp8_quantize_1x128_e5m2(x: torch.Tensor, q: torch.Tensor, sA: torch.Tensor) 
     _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1,
           "sA: f32 [K/128, ld_sa]")
     ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(sA.shape[1] >= M, "sA: f32 [K/128, ld_sa >= M]")
+    _on_one_device(x, q, sA)
     _check(lib().fp8_quantize_1x128_e5m2(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(sA), ld_sa,
                                          _stream(x)), "fp8_quantize_1x128_e5m2")
 
@@ -301,10 +346,11 @@ def fp8_gemm_nt_dgrad(A, sA, B, sB, D) -> None:
     _need(A.dtype in (torch.uint8, torch.float8_e5m2) and A.dim() == 2 and A.stride(1) == 1, "A: e5m2 [M,K]")
     _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
     _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
-    _need(sA.dtype == torch.float32 and sB.dtype == torch.float32 and sB.is_contiguous(), "scales: f32")
     M, K = A.shape
     N = B.shape[0]
-    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(B.shape[1] == K and D.shape == (M, N), "shapes: A [M,K], B [N,K], D [M,N]")
+    ld_sa = _block_scales(sA, sB, M, N, K, 1)
+    _on_one_device(A, sA, B, sB, D)
     _check(lib().fp8_gemm_nt_dgrad(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
                                    _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt_dgrad")
 
@@ -315,10 +361,13 @@ def fp8_grouped_gemm_contiguous_dgrad(A, sA, B, sB, D, group_offsets) -> None:
           "A: e5m2 [M_total,K] contiguous")
     _need(_is_fp8(B) and B.dim() == 3 and B.is_contiguous(), "B: e4m3 [E,N,K] contiguous")
     _need(D.dtype == torch.bfloat16 and D.is_contiguous(), "D: bf16 [M_total,N] contiguous")
-    _need(group_offsets.dtype == torch.int32 and group_offsets.is_cuda, "group_offsets: int32 device tensor")
+    _need(group_offsets.dtype == torch.int32, "group_offsets: int32 device tensor")
     M_total, K = A.shape
     E, N, _ = B.shape
-    ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
+    _need(B.shape[2] == K and D.shape == (M_total, N) and group_offsets.numel() == E + 1,
+          "shapes: A [M_total,K], B [E,N,K], D [M_total,N], group_offsets [E+1]")
+    ld_sa = _block_scales(sA, sB, M_total, N, K, E)
+    _on_one_device(A, sA, B, sB, D, group_offsets)
     _check(lib().fp8_grouped_gemm_contiguous_dgrad(_ptr(A), _ptr(sA), ld_sa, _ptr(B), _ptr(sB), _ptr(D),
                                                    _ptr(group_offsets), E, M_total, N, K, _stream(A)),
            "fp8_grouped_gemm_contiguous_dgrad")
@@ -330,13 +379,18 @@ def fp8_grouped_gemm_wgrad(A, sA, B, sB, D, offsets) -> None:
     _need(A.dtype in (torch.uint8, torch.float8_e5m2) and A.dim() == 2 and A.stride(1) == 1, "A: e5m2 [M,T]")
     _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,T]")
     _need(D.dtype == torch.bfloat16 and D.dim() == 3 and D.is_contiguous(), "D: bf16 [E,M,N] contiguous")
-    _need(offsets.dtype == torch.int32 and offsets.is_cuda, "offsets: int32 device tensor")
+    _need(offsets.dtype == torch.int32, "offsets: int32 device tensor")
     M, T = A.shape
     N = B.shape[0]
     E = D.shape[0]
-    _need(offsets.numel() == E + 1 and D.shape[1:] == (M, N), "shapes")
+    _need(B.shape[1] == T and offsets.numel() == E + 1 and D.shape[1:] == (M, N), "shapes")
+    for t, rows, name in ((sA, M, "sA"), (sB, N, "sB")):
+        _need(t.dtype == torch.float32 and t.dim() == 2 and t.shape[0] == T // 128 and t.stride(1) == 1
+              and t.shape[1] >= rows and (t.shape[0] == 1 or t.stride(0) >= t.shape[1]),
+              f"{name}: f32 [T/128, ld >= {rows}]")
     ld_sa = sA.stride(0) if sA.shape[0] > 1 else sA.shape[1]
     ld_sb = sB.stride(0) if sB.shape[0] > 1 else sB.shape[1]
+    _on_one_device(A, sA, B, sB, D, offsets)
     _check(lib().fp8_grouped_gemm_wgrad(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
                                         ld_sb, _ptr(D), _ptr(offsets), E, M, N, T, _stream(A)),
            "fp8_grouped_gemm_wgrad")
@@ -348,9 +402,11 @@ def fp8g_get_status(stream: torch.cuda.Stream | None = None) -> int:
 
 
 def fp8g_last_config() -> dict:
-    bn, st, gr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    """Tile width, stages, grid and whether the tail was split (stream-K) of this thread's last GEMM."""
+    bn, st, gr, sp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     _check(lib().fp8g_last_config(ctypes.byref(bn), ctypes.byref(st), ctypes.byref(gr)), "fp8g_last_config")
-    return {"block_n": bn.value, "stages": st.value, "grid": gr.value}
+    _check(lib().fp8g_last_split(ctypes.byref(sp)), "fp8g_last_split")
+    return {"block_n": bn.value, "stages": st.value, "grid": gr.value, "split": bool(sp.value)}
 
 
 # ------------------------------------------------------------------ allocating wrappers

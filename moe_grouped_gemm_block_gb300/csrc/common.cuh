@@ -32,6 +32,16 @@ long long wait_budget_cycles();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Stream-K workspace: one FP32 partial-tile slot per SM (128 rows x 256 columns at most) and one
+// flag per SM.  fp8_gemm_nt_noalloc uses a fixed scratch holding kNoAllocSlots slots and
+// kNoAllocFlagBytes of flags (noalloc.cu); noalloc_scratch() returns its device address on `dev`
+// (the current device), or null if the lookup failed.
+constexpr size_t kSkSlotBytes = static_cast<size_t>(128) * 256 * 4;
+constexpr int kNoAllocSlots = 160;
+constexpr size_t kNoAllocFlagBytes = 1024;
+constexpr size_t kNoAllocBytes = kSkSlotBytes * kNoAllocSlots + kNoAllocFlagBytes;
+void* noalloc_scratch(int dev);
+
 // Device-side: record the first error code in the status word.
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int code) {
   atomicCAS(status, 0u, code);

@@ -63,7 +63,6 @@ enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3, kK
 constexpr int BM = 128;  // rows per tile = TMEM lanes
 constexpr int BK = 128;  // K per stage = the scaling block
 constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a band)
-constexpr int kSAAhead = 4;  // K-block steps by which the A-row scales are loaded ahead
 
 // PAIR: a cluster of two CTAs computes 256 x BN tiles with tcgen05.mma.cta_group::2; each CTA
 // loads its 128 A rows and half of the B tile (BN / 2 rows), so a stage is 32 KB and six fit.
@@ -73,7 +72,9 @@ constexpr int kSAAhead = 4;  // K-block steps by which the A-row scales are load
 // warp's 512 bytes of per-column B scales.
 template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
 struct Cfg {
-  static constexpr int kEpiCols = BN >= 128 ? 128 : BN;  // columns per epilogue warp
+  // columns per epilogue warp.  256 x 128 pair tiles: 64, so that each warp reads its whole
+  // partial with one load and frees the TMEM buffer before any FMA.
+  static constexpr int kEpiCols = (PAIR && BN == 128) ? 64 : (BN >= 128 ? 128 : BN);
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
   // Narrow tiles (few, long K loops: small-M shapes) split the K blocks between two sets of
   // promotion warps (even / odd K blocks), whose FP32 partial sums are added at the tile end.
@@ -85,7 +86,8 @@ struct Cfg {
   // One thread pays ~60 cycles per tcgen05.mma plus ~170 per mbarrier round trip, which caps
   // the narrow small-M tiles (whose MMAs are short); there two issuers share the stream.
   // Wider tiles keep one: their MMAs are long enough, and measured slower with two.
-  static constexpr int kMmaWarps = SMALL ? 2 : 1;
+  // 256 x 128 pair tiles: four MMAs of ~64 cycles per K block for the pair, so two lone issuers.
+  static constexpr int kMmaWarps = (SMALL || (PAIR && BN == 128)) ? 2 : 1;
   // BN = 256: three full warpgroups (producer / 2 MMA / idle, then 2 epilogue warpgroups) so
   // that setmaxnreg can move registers to the epilogue: the launch gives 384 x 168 = 64512,
   // rebalanced to 128 x 40 + 256 x 232 = 64512.  Otherwise: producer and MMA warps, then the
@@ -102,7 +104,7 @@ struct Cfg {
   // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
   static constexpr int kKPS = SMALL ? 2 : 1;
   static constexpr int kStages =
-      SMALL ? 6 : (PAIR ? (BN == 256 ? 6 : 8) : (KG ? 3 : (BN == 256 ? 4 : 6)));
+      SMALL ? 6 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN == 256 ? 4 : 6)));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
@@ -115,20 +117,29 @@ struct Cfg {
   static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box
   static constexpr int kOutBoxes = KG ? kEpiCols / 32 : 1;  // staging boxes per store warp
   static constexpr uint32_t kOutWarpBytes = kOutBoxes * kOutBytes;
-  static constexpr uint32_t kSbvBytes = KG ? 512u * kEpiWarps : 0u;  // per-column B scales
+  // K-grouped: the scales of each stage's K block, staged next to its operands by the producer --
+  // the tile's 128 A-row scales (a 512-byte TMA box) and its BN per-column B scales (a TMA box).
+  // (The block forms read their two scales per K block from global memory, well ahead of use.)
+  static constexpr uint32_t kSAKB = BM * 4;
+  static constexpr uint32_t kSBKB = BN * 4;
+  static constexpr uint32_t kScaleStage = KG ? kSAKB + kSBKB : 0u;
+  // K-grouped: each epilogue warp copies its 128 columns' B scales out of the stage (512 bytes)
+  static constexpr uint32_t kSbvBytes = KG ? 512u * kEpiWarps : 0u;
   static constexpr int kXRows = SMALL ? 64 : BM;
   static constexpr uint32_t kXBytes = kKSplit > 1 ? kXRows * BN * 4 : 0;  // K-split exchange
   // shared-memory carve-up (offsets from a 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kStageABytes;
   static constexpr uint32_t kOffOut = kOffB + kStages * kStageBBytes;
-  static constexpr uint32_t kOffSbv = kOffOut + kStoreWarps * kOutWarpBytes;
+  static constexpr uint32_t kOffScale = kOffOut + kStoreWarps * kOutWarpBytes;
+  static constexpr uint32_t kOffSbv = kOffScale + kStages * kScaleStage;
   static constexpr uint32_t kOffX = kOffSbv + kSbvBytes;
   static constexpr uint32_t kOffBar = kOffX + kXBytes;
-  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kTmemBufs + 4;
+  static constexpr uint32_t kNumBars = 3 * kStages + 2 * kTmemBufs + 4;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
+  static_assert(kOffScale % 128 == 0 && kScaleStage % 128 == 0 && kOffSbv % 16 == 0, "scale staging alignment");
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
@@ -426,8 +437,8 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* f, const GemmArgs& a, 
 template <int BN, int MODE, bool PAIR = false, bool EPI = false>
 __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmD,
-                    const GemmArgs a) {
+                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmSB, const GemmArgs a) {
   using C = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>;
   static_assert(!EPI || (C::kKSplit == 1 && C::kMmaWarps == 1 && !PAIR),
                 "epilogue scaling: one K part, one issuer, single-CTA tiles");
@@ -453,6 +464,15 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
   const uint32_t xempty = xfull + 8u;                             // K-split exchange read
   const uint32_t sk_written = xfull + 16u;  // stream-K: every epilogue warp has written its partial
   const uint32_t sk_ready = xfull + 24u;    // stream-K: the partials to add are complete
+  // the scales of stage s have landed (K-grouped form)
+  auto sfull = [&](uint32_t st) { return xfull + 32u + 8u * st; };
+  constexpr bool kStaged = MODE == kKGrouped;
+  // Arrivals that free an operand stage: the MMA commit (lone issuers, CTA pairs and the
+  // epilogue-scaled variant); else one lane of the promotion warps once the stage's MMAs have
+  // completed (block forms), or every promotion warp once it has also read the stage's scales
+  // (K-grouped).
+  constexpr bool kCommitFrees = EPI || C::kMmaWarps > 1 || PAIR;
+  constexpr uint32_t kEmptyArrivals = kCommitFrees ? 1u : (kStaged ? static_cast<uint32_t>(C::kEpiWarps) : 1u);
   // misc: [0] TMEM base, [1] abort flag, [2] group table out of contract
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -461,7 +481,8 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);  // the commit of the stage's issuer
+      mbar_init(empty(s), kEmptyArrivals);
+      mbar_init(sfull(s), 1);  // the producer's expect-tx arrival
     }
     // each TMEM buffer is consumed by the warps of one K part
     for (uint32_t b = 0; b < NB; ++b) {
@@ -479,6 +500,10 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmD);
+    if (kStaged) {
+      prefetch_tmap(&tmSA);
+      prefetch_tmap(&tmSB);
+    }
   }
   if (warp == 1) {
     if constexpr (PAIR) {  // one warp of each CTA of the pair, collectively
@@ -581,17 +606,17 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
     const bool leader = lane == 0;
     constexpr int KPS = C::kKPS;
     constexpr int MW = C::kMmaWarps;
-    // One issuer (wide tiles): the producer and MMA warps run their loops with all 32 lanes
-    // (warp-uniform control flow and operands), lane 0 issuing; the epilogue frees each stage
-    // when it sees the stage's partial.  Two issuers (small-M tiles): lane 0 alone runs each
-    // loop, tests its next barriers ahead (wait_seen) and frees stages by an MMA commit.  Each
-    // form measured faster where it is used.
+    // Lane 0 of the producer warp runs its loop alone.  One MMA issuer (wide tiles) runs its loop
+    // with all 32 lanes (lane 0 issuing), each lane testing the barriers itself, without a warp
+    // vote after each wait: measured per K block on 4096 x 8192 x 8192, ~850 cycles against ~900
+    // with the vote and ~935 with lane 0 alone.  Two issuers (small-M tiles, 256 x 128 pair tiles)
+    // run on lane 0 alone, test their next barriers ahead (wait_seen) and free stages by an MMA
+    // commit; one issuer leaves the stage release to the promotion warps.
     constexpr bool kLone = MW > 1;
     static_assert(KPS == 1 || kLone, "multi-K-block stages are freed by the issuers' commits");
-    static_assert(!kLone || !PAIR, "CTA pairs have one issuer");
     // the tensor maps view A as [K/128][rows][128] and B as [E][K/128][N][128] (outer to
     // inner), so one box holds KPS K blocks of the tile's rows, K block by K block
-    if (warp == 0 && (!kLone || leader)) {
+    if (warp == 0 && leader) {
       // ---------------------------------------------------------- TMA producer
       uint32_t it = 0;  // stages filled
       bool ok = true;
@@ -609,7 +634,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
             ready = wait_seen(empty_seen, empty(s), ph ^ 1u, a, abort_flag);
             empty_seen = mbar_test_wait(empty((it + 1) % S), (((it + 1) / S) & 1u) ^ 1u);
           } else {
-            ready = __all_sync(0xffffffffu, wait_bounded(empty(s), ph ^ 1u, a, abort_flag));
+            ready = wait_bounded(empty(s), ph ^ 1u, a, abort_flag);
           }
           if (!ready) { ok = false; break; }
           const uint32_t dA = base + C::kOffA + s * C::kStageABytes;
@@ -624,6 +649,13 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
             mbar_arrive_expect_tx(leader, full(s), C::kStageABytes + C::kStageBBytes);
             tma_load_3d(leader, dA, &tmA, full(s), 0, ti.a_row, ti.kb_first + kb);
             tma_load_4d(leader, dB, &tmB, full(s), 0, ti.n0, ti.kb_first + kb, MODE == kKGrouped ? 0 : ti.g);
+          }
+          if constexpr (kStaged) {
+            // the tile's A-row scales (rows past the matrix read as zero) and its per-column B scales
+            const uint32_t dS = base + C::kOffScale + s * C::kScaleStage;
+            mbar_arrive_expect_tx(leader, sfull(s), C::kSAKB + C::kSBKB);
+            tma_load_2d(leader, dS, &tmSA, sfull(s), ti.a_row, ti.kb_first + kb);
+            tma_load_2d(leader, dS + C::kSAKB, &tmSB, sfull(s), ti.n0, ti.kb_first + kb);
           }
         }
       }
@@ -654,12 +686,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
           if (!fetch_tile(pc, ti)) continue;
           const uint32_t b = np % NB, tph = (np / NB) & 1u;
           ++np;
-          if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
+          if (!(wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * BN;
           for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
             const uint32_t s = it % S, ph = (it / S) & 1u;
-            if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
+            if (!(wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
             tc_fence_after();
             const uint64_t ad = adesc0 + ((s * C::kStageABytes) >> 4);
             const uint64_t bd = bdesc0 + ((s * C::kStageBBytes) >> 4);
@@ -688,8 +720,10 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
           for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
             const uint32_t s = it % S, ph = (it / S) & 1u;
             const uint32_t b = it % NB, tph = (it / NB) & 1u;
-            if (!__all_sync(0xffffffffu, wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
-            if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
+            // the operand stage first: it is nearly always complete, and testing it costs a round
+            // trip that would otherwise sit between the buffer's release and the MMAs
+            if (!(wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
+            if (!(wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
             tc_fence_after();
             const uint64_t ad = adesc0 + ((s * C::kStageABytes) >> 4);
             const uint64_t bd = bdesc0 + ((s * C::kStageBBytes) >> 4);
@@ -704,7 +738,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
 #pragma unroll
               for (int k = 0; k < BK / 32; ++k)
                 mma_f8f6f4(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-              // one commit per K block: the epilogue, on seeing the partial, also frees the stage
+              // one commit per K block; the promotion warps free the stage once it has completed
               mma_commit(leader, tfull(b));
             }
           }
@@ -755,16 +789,25 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
                 const uint64_t ad = adesc0 + ((s * C::kStageABytes + j * C::kABytes) >> 4);
                 const uint64_t bd = bdesc0 + ((s * C::kStageBBytes + j * C::kBBytes) >> 4);
                 const uint32_t d_tmem = tmem_base + b * BN;
+                if constexpr (PAIR) {  // rank 0 issues for the pair; both CTAs' partials are ready
 #pragma unroll
-                for (int k = 0; k < BK / 32; ++k)
-                  mma_f8f6f4(true, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-                mma_commit(true, tfull(b));
+                  for (int k = 0; k < BK / 32; ++k)
+                    mma_f8f6f4_pair(true, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                  mma_commit_pair(true, tfull(b), 0x3);
+                } else {
+#pragma unroll
+                  for (int k = 0; k < BK / 32; ++k)
+                    mma_f8f6f4(true, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                  mma_commit(true, tfull(b));
+                }
                 issued = true;
                 last_bar = tfull(b);
                 last_ph = tph;
               }
               if (!ok) break;
-              mma_commit(true, empty(s));  // the stage is free once these MMAs have read it
+              // the stage is free once these MMAs have read it (in a pair: both CTAs' stages)
+              if constexpr (PAIR) mma_commit_pair(true, empty(s), 0x3);
+              else mma_commit(true, empty(s));
             }
             kit += nk;
           }
@@ -786,10 +829,6 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
     const int kpart = grp / C::kColGroups;                 // promotes K blocks kb % kKSplit == kpart
     const int col0 = (grp % C::kColGroups) * C::kEpiCols;  // column offset inside the tile
     const int row = q * 32 + lane;       // tile row owned by this thread
-    // one issuer: one lane per K part frees the operand stage of each K block once its MMAs
-    // are done (the tile's K blocks map one to one onto stages)
-    const bool stage_releaser =
-        !EPI && C::kMmaWarps == 1 && !PAIR && lane == 0 && ew == kpart * 4 * C::kColGroups;
     // this warp's TMEM buffers are released on rank 0's barrier (its own CTA unless paired)
     auto release_tmem = [&](uint32_t b) {
       if (lane == 0) {
@@ -839,70 +878,50 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
         __syncwarp();
         release_tmem(b);
       } else {
-        // (K-grouped: the B scales are one per column and K block, read per K block below)
-        const bool blk_sb = MODE != kKGrouped && has_cols;
-        const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
-        // B scales of this column block: lane i holds the one of K block sb_base + i (sb_cur)
-        // and sb_base + 32 + i (sb_nxt), broadcast by shuffle.
-        int32_t sb_base = pc.kb0 & ~31;
-        float sb_cur = (blk_sb && sb_base + lane < a.KB) ? ld_nc_f32(sbp + sb_base + lane) : 0.0f;
-        float sb_nxt = (blk_sb && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
-        // A-row scale of this thread's row, read from global memory kSAAhead K-block steps
-        // before use (coalesced: a warp reads 32 consecutive rows of one K block)
-        const float* sap = a.sA + static_cast<int64_t>(ti.kb_first) * a.ld_sa + grow;
-        float sa_q[kSAAhead];
-#pragma unroll
-        for (int i = 0; i < kSAAhead; ++i) {
-          const int32_t kbi = pc.kb0 + kpart + i * C::kKSplit;
-          sa_q[i] = (row_ok && kbi < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbi) * a.ld_sa) : 0.0f;
-        }
+        // Per K block: acc += P * (sa * sb), with the partial P from TMEM.
+        //   Block forms: sa (this thread's row) and sb (this warp's 128-column block) come from
+        //   global memory two K-block steps ahead of use, in two register pairs used alternately:
+        //   the loop below is unrolled by two, so a pair is touched only by its load and, two
+        //   steps later, its use (no wait on a load in between, and no barrier or shared-memory
+        //   round trip per K block).
+        //   K-grouped: sa and the per-column B scales from the stage's scales in shared memory.
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-        // K-grouped: the B scales of this warp's columns for one K block, lane l loading columns
-        // 4l .. 4l+3 (one coalesced 16-byte load per lane, a K block ahead), staged in this warp's
-        // 512 bytes of shared memory and read back with warp-uniform addresses.
-        auto load_sbv = [&](int32_t kbi) {
-          float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (MODE == kKGrouped && kbi < pc.kb1 && ncol0 + 4 * lane < a.N)
-            r = __ldg(reinterpret_cast<const float4*>(a.sB + static_cast<int64_t>(ti.kb_first + kbi) * a.ld_sb +
-                                                      ncol0) + lane);
-          return r;
+        constexpr int KS = C::kKSplit;
+        const float* sap = a.sA + static_cast<int64_t>(ti.kb_first) * a.ld_sa + grow;
+        const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
+        const bool blk_sb = MODE != kKGrouped && has_cols;
+        auto load_scales = [&](int32_t kbi, float& sa_o, float& sb_o) {
+          sa_o = ld_nc_f32_or0(sap + static_cast<int64_t>(kbi) * a.ld_sa, MODE != kKGrouped && row_ok && kbi < pc.kb1);
+          sb_o = ld_nc_f32_or0(sbp + kbi, blk_sb && kbi < pc.kb1);
         };
-        float4 sbv_nxt = load_sbv(pc.kb0 + kpart);
+        float sa0, sb0, sa1, sb1;
+        load_scales(pc.kb0 + kpart, sa0, sb0);
+        load_scales(pc.kb0 + kpart + KS, sa1, sb1);
         // What sets the pace of the wide tiles: a TMEM buffer is written again (K block kb + NB)
         // only after all of its warps have loaded it, so each K block's MMA, its completion, these
-        // loads and the release form a chain that NB = 2 buffers must cover.  Measured at BN = 256:
-        // ~930 cycles per K block against 520 of MMA; each warp's own loads and FMAs take ~770 of
-        // them, and the next partial is rarely complete when a warp finishes the current one (an
-        // early test of its barrier measured slower).
-        for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += C::kKSplit) {
-          if (MODE == kKGrouped) {
-            __syncwarp();  // every lane has read the previous K block's scales
-            st_shared_v4(sbv_addr + 16 * lane, __float_as_uint(sbv_nxt.x), __float_as_uint(sbv_nxt.y),
-                         __float_as_uint(sbv_nxt.z), __float_as_uint(sbv_nxt.w));
-            __syncwarp();
-          }
-          sbv_nxt = load_sbv(kb + C::kKSplit);
+        // loads and the release form a chain that NB = 2 buffers must cover.
+        auto step = [&](int32_t kb, float& sa_r, float& sb_r) -> bool {
           const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
           const uint32_t b = it % NB, tph = (it / NB) & 1u;
-          const float sa_kb = sa_q[0];
-#pragma unroll
-          for (int i = 0; i + 1 < kSAAhead; ++i) sa_q[i] = sa_q[i + 1];
-          {
-            const int32_t kbn = kb + kSAAhead * C::kKSplit;
-            sa_q[kSAAhead - 1] =
-                (row_ok && kbn < pc.kb1) ? ld_nc_f32(sap + static_cast<int64_t>(kbn) * a.ld_sa) : 0.0f;
+          const uint32_t s = it % S, sph = (it / S) & 1u;  // (one K block per stage)
+          float sa_kb = sa_r, sb_kb = sb_r;
+          load_scales(kb + 2 * KS, sa_r, sb_r);
+          if constexpr (MODE == kKGrouped) {
+            // the stage's scales land long before its partial: take them first
+            if (!__all_sync(0xffffffffu, wait_bounded(sfull(s), sph, a, abort_flag))) return false;
+            const uint32_t sc = base + C::kOffScale + s * C::kScaleStage;
+            sa_kb = ld_shared_f32(sc + 4u * static_cast<uint32_t>(row));
+            // lane l: the B scales of columns col0 + 4l .. 4l+3, copied into this warp's own area
+            const float4 v = ld_shared_v4f(sc + C::kSAKB + 4u * static_cast<uint32_t>(col0) + 16u * lane);
+            __syncwarp();  // every lane has read the previous K block's copy
+            st_shared_v4(sbv_addr + 16 * lane, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                         __float_as_uint(v.w));
+            __syncwarp();
           }
-          if (kb >= sb_base + 32) {
-            sb_base += 32;
-            sb_cur = sb_nxt;
-            sb_nxt = (blk_sb && sb_base + 32 + lane < a.KB) ? ld_nc_f32(sbp + sb_base + 32 + lane) : 0.0f;
-          }
-          const float sb_kb = __shfl_sync(0xffffffffu, sb_cur, kb - sb_base);
           const float scale = sa_kb * sb_kb;
           const float2 scale2 = make_float2(scale, scale);
-          if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
-          if (stage_releaser) mbar_arrive(empty(it % S));
+          if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) return false;
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
           if (live) {
@@ -938,6 +957,19 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
             __syncwarp();
             release_tmem(b);
           }
+          // Free the operand stage (one K block per stage in these forms) once its MMAs are known
+          // complete -- here, after the TMEM release, off the path from the partial to the next
+          // MMAs.  K-grouped: every warp, having read the stage's scales; else the first warp of
+          // each K part (lone issuers, pairs and the epilogue-scaled variant free stages by commit).
+          if constexpr (!kCommitFrees) {
+            if (lane == 0 && (kStaged || ew == kpart * 4 * C::kColGroups)) mbar_arrive(empty(s));
+          }
+          return true;
+        };
+        for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += 2 * KS) {
+          if (!step(kb, sa0, sb0)) { ok = false; break; }
+          if (kb + KS >= pc.kb1) break;
+          if (!step(kb + KS, sa1, sb1)) { ok = false; break; }
         }
       }
       it_base += static_cast<uint32_t>(pc.kb1 - pc.kb0);
@@ -1127,8 +1159,8 @@ static_assert(Cfg<128, false, false, true>::kOffTable + 4 * (kMaxExperts + 1) <=
 
 template <int BN, int MODE, bool PAIR = false, bool EPI = false>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
-                  const CUtensorMap& tD, int grid, int table_entries,
-                  cudaStream_t stream) {
+                  const CUtensorMap& tD, const CUtensorMap& tSA, const CUtensorMap& tSB, int grid,
+                  int table_entries, cudaStream_t stream) {
   using C = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>;
   auto kern = fp8_gemm_kernel<BN, MODE, PAIR, EPI>;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
@@ -1169,7 +1201,7 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, args) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, tSA, tSB, args) != cudaSuccess) {
       cudaGetLastError();
       return FP8G_ERR_CUDA;
     }
@@ -1188,21 +1220,22 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, args) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, tSA, tSB, args) != cudaSuccess) {
       cudaGetLastError();
       return FP8G_ERR_CUDA;
     }
     return FP8G_OK;
   }
-  kern<<<grid, C::kThreads, smem, stream>>>(tA, tB, tD, args);
+  kern<<<grid, C::kThreads, smem, stream>>>(tA, tB, tD, tSA, tSB, args);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
 // Stream-K workspace: one per (device, stream), allocated on the first call that needs it and
 // kept for the life of the process.  Per stream, because launches on different streams may run
 // at the same time; launches on one stream run in order and reuse it.  It holds one FP32
-// partial-tile slot per SM (128 x 128 columns x 2 column groups at most) and one flag per SM.
-constexpr size_t kSkSlotBytes = static_cast<size_t>(BM) * 256 * 4;
+// partial-tile slot per SM (kSkSlotBytes: 128 x 128 columns x 2 column groups at most) and one
+// flag per SM.
+static_assert(kSkSlotBytes == static_cast<size_t>(BM) * 256 * 4, "stream-K slot size");
 struct SkWorkspace {
   void* base = nullptr;
   size_t flag_offset = 0;
@@ -1244,30 +1277,7 @@ bool env_streamk() {
   return !(e && e[0] == '0' && e[1] == 0);
 }
 
-// Fixed scratch of fp8_gemm_nt_noalloc: the stream-K slots of up to kNoAllocSlots SMs, then the
-// flags.  Part of the library's device image, so using it allocates nothing.
-constexpr int kNoAllocSlots = 160;
-constexpr size_t kNoAllocFlagBytes = 1024;
-constexpr size_t kNoAllocBytes = kSkSlotBytes * kNoAllocSlots + kNoAllocFlagBytes;
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
-
-constexpr int kNoAllocDevices = 64;
-std::once_flag g_noalloc_once[kNoAllocDevices];
-void* g_noalloc_addr[kNoAllocDevices] = {};
-
-// Device address of the fixed scratch on device `dev` (the current device), looked up on the
-// first call for that device; null if the lookup failed.
-void* noalloc_scratch(int dev) {
-  if (dev < 0 || dev >= kNoAllocDevices) return nullptr;
-  std::call_once(g_noalloc_once[dev], [dev] {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) g_noalloc_addr[dev] = p;
-    else cudaGetLastError();
-  });
-  return g_noalloc_addr[dev];
-}
-
-thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0;
+thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0, t_last_split = 0;
 
 // FP8G_PAIR=1 runs 256-wide tiles as 256 x 256 CTA-pair tiles, FP8G_PAIR=2 as 256 x 128 pair
 // tiles (four TMEM partial buffers per CTA).  Off by default: measured no faster than single-CTA
@@ -1388,6 +1398,27 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
       return st;
   }
+  // Scales staged per stage (block-scaled forms): sA as [K/128][rows] fp32 with row stride ld_sa,
+  // a box being the 128 A-row scales of a tile for kps K blocks (rows past the matrix read as
+  // zero); K-grouped: the per-column B scales as [T/128][N] (row stride ld_sb), a box of BN.
+  // The epilogue-scaled variant reads its scales directly; its maps are unused placeholders.
+  CUtensorMap tSA = tA, tSB = tA;
+  if (!EPI) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(o.rows), static_cast<uint64_t>(o.K / BK)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(o.ld_sa) * 4};
+    const uint32_t box[2] = {static_cast<uint32_t>(BM), kps};
+    if ((st = encode_tmap(&tSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, o.sA, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != FP8G_OK)
+      return st;
+  }
+  if (MODE == kKGrouped) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.K / BK)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(o.ld_sb) * 4};
+    const uint32_t box[2] = {static_cast<uint32_t>(bn), 1};
+    if ((st = encode_tmap(&tSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, o.sB, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != FP8G_OK)
+      return st;
+  }
   {
     // D: [rows, N] (K-grouped: one [rows, N] matrix per expert, stacked)
     const uint64_t d_rows = static_cast<uint64_t>(MODE == kKGrouped ? o.E * o.rows : o.rows);
@@ -1451,47 +1482,48 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
 
   t_last_bn = bn;
   t_last_grid = grid;
+  t_last_split = a.sk;
   if constexpr (MODE == kKGrouped) {
     if (bn == 256) {
       t_last_stages = Cfg<256, false, false, true>::kStages;
-      return launch_kernel<256, kKGrouped>(a, tA, tB, tD, grid, table_entries, stream);
+      return launch_kernel<256, kKGrouped>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
     }
     t_last_stages = Cfg<128, false, false, true>::kStages;
-    return launch_kernel<128, kKGrouped>(a, tA, tB, tD, grid, table_entries, stream);
+    return launch_kernel<128, kKGrouped>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
   } else if constexpr (EPI) {
     if (bn == 256) {
       t_last_stages = Cfg<256>::kStages;
-      return launch_kernel<256, MODE, false, true>(a, tA, tB, tD, grid, table_entries, stream);
+      return launch_kernel<256, MODE, false, true>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
     }
     t_last_stages = Cfg<128>::kStages;
-    return launch_kernel<128, MODE, false, true>(a, tA, tB, tD, grid, table_entries, stream);
+    return launch_kernel<128, MODE, false, true>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
   } else {
     switch (bn) {
       case 256:
         if (pair) {
           t_last_stages = Cfg<256, false, true>::kStages;
-          return launch_kernel<256, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
+          return launch_kernel<256, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, tSA, tSB, grid,
                                                                                  table_entries, stream);
         }
         t_last_stages = Cfg<256>::kStages;
-        return launch_kernel<256, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+        return launch_kernel<256, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
       case 128:
         if (pair) {
           t_last_stages = Cfg<128, false, true>::kStages;
-          return launch_kernel<128, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, grid,
+          return launch_kernel<128, (MODE == kDenseSmallM ? kDense : MODE), true>(a, tA, tB, tD, tSA, tSB, grid,
                                                                                  table_entries, stream);
         }
         t_last_stages = Cfg<128>::kStages;
-        return launch_kernel<128, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+        return launch_kernel<128, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
       default:
         if constexpr (MODE == kDense) {
           if (small_m) {
             t_last_stages = Cfg<64, true>::kStages;
-            return launch_kernel<64, kDenseSmallM>(a, tA, tB, tD, grid, table_entries, stream);
+            return launch_kernel<64, kDenseSmallM>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
           }
         }
         t_last_stages = Cfg<64>::kStages;
-        return launch_kernel<64, MODE>(a, tA, tB, tD, grid, table_entries, stream);
+        return launch_kernel<64, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
     }
   }
 }
@@ -1711,6 +1743,12 @@ extern "C" int fp8g_selftest_bounded_waits(int64_t budget_cycles, uint32_t* out,
   a.budget = budget_cycles;
   bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(a, out);
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+}
+
+extern "C" int fp8g_last_split(int* split) {
+  if (!split) return FP8G_ERR_INVALID_ARG;
+  *split = t_last_split;
+  return FP8G_OK;
 }
 
 extern "C" int fp8g_last_config(int* block_n, int* stages, int* grid) {

@@ -72,7 +72,7 @@ def test_dense_256_wide_single_cta_and_pair(M, N, K, use_pair):
         D = _dense_gpu(qa, sa, qb, sb, 256)
         cfg = g.fp8g_last_config()
     paired = use_pair and M > 128  # a single m-block never runs as a pair
-    want = {0: (256, 4), 1: (256, 6), 2: (128, 8)}[use_pair if paired else 0]
+    want = {0: (256, 4), 1: (256, 5), 2: (128, 8)}[use_pair if paired else 0]
     assert (cfg["block_n"], cfg["stages"]) == want
     assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"{M}x{N}x{K} pair={use_pair}")
 

@@ -22,19 +22,28 @@ def _operands(M, N, K, seed):
     return qa, sa, qb, sb
 
 
-# 640x768x4096: 15 tiles, every one split across 4 SMs (the scratch is used);
+# 640x768x4096: 15 tiles, every one split across several SMs (the scratch is used);
 # 2560x2048x4096: a whole round of tiles, then 8 split tiles;  64x1024x512: no split at all
-@pytest.mark.parametrize("M,N,K", [(640, 768, 4096), (2560, 2048, 4096), (64, 1024, 512)])
-def test_noalloc_equals_the_allocating_call_on_two_calls_in_a_row(M, N, K):
+@pytest.mark.parametrize("M,N,K,splits", [(640, 768, 4096, True), (2560, 2048, 4096, True), (64, 1024, 512, False)])
+def test_noalloc_equals_the_allocating_call_on_two_calls_in_a_row(M, N, K, splits):
     need_gpu()
     qa, sa, qb, sb = _operands(M, N, K, seed=M + N + K)
     A, SA, B, SB = u8(qa), sa_to_device(sa), u8(qb), torch.from_numpy(sb).cuda()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     outs = {}
     with block_n(256 if M > 64 else None):
         for name, fn in (("alloc", g.fp8_gemm_nt), ("noalloc", g.fp8_gemm_nt_noalloc)):
             for i in range(2):
                 D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
                 fn(A, SA, B, SB, D)
+                cfg = g.fp8g_last_config()
+                # the split tail (which works in the fixed scratch) ran exactly where expected: on
+                # every SM, or on fewer SMs than tiles-or-SMs without a split
+                assert cfg["split"] == splits, (name, cfg)
+                if splits:
+                    assert cfg["grid"] == sms, (name, cfg)
+                else:
+                    assert cfg["grid"] < sms, (name, cfg)
                 outs[(name, i)] = D
     torch.cuda.synchronize()
     check_status()
