@@ -158,11 +158,53 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, uint32_t d
   return make_uint2(w[0], w[1]);
 }
 
+// s = RN(amax / c) for c = 7 * 2^k (448, 57344) without a division: q = RN(amax * RN(1/c)) is
+// within about one ulp of the quotient, so the nearest of q and its two neighbours is RN(amax / c).
+// Their residuals amax - c * q' are exact in one FMA (amax has 8 significant bits and c * q' lies
+// within a few ulps of it), and no quotient of a bf16 value by 7 * 2^k lies halfway between two
+// floats (it is either exact or has a non-terminating binary expansion), so the smallest residual
+// decides without ties.  Results below the normal range (amax < c * 2^-126) take the division.
+// (An exhaustive check over every bf16 significand and exponent is in the tests.)
+template <int FMT>
+__device__ __forceinline__ float block_scale(float amax) {
+  constexpr float c = FMT == kE5M2 ? kE5M2Max : kE4M3Max;
+  constexpr float r = 1.0f / c;  // RN(1/c), folded by the compiler
+  if (!(amax >= c * 1.17549435e-38f)) return __fdiv_rn(amax, c);  // zero, subnormal results
+  const float q = __fmul_rn(amax, r);
+  const float qd = __uint_as_float(__float_as_uint(q) - 1u), qu = __uint_as_float(__float_as_uint(q) + 1u);
+  const float e = fabsf(__fmaf_rn(-c, q, amax)), ed = fabsf(__fmaf_rn(-c, qd, amax)),
+              eu = fabsf(__fmaf_rn(-c, qu, amax));
+  float best = q, eb = e;
+  if (ed < eb) { best = qd; eb = ed; }
+  if (eu < eb) best = qu;
+  return best;
+}
+
 // Eight lanes per (row, 128-wide K block); lane i of the group holds values 8i..8i+7 and
-// 64+8i..64+8i+7, so each 16-byte load instruction of a warp reads four whole 128-byte
-// lines.  Each group keeps kQUnroll blocks in flight to cover HBM latency.
-constexpr int kQThreads = 256;
-constexpr int kQUnroll = 2;
+// 64+8i..64+8i+7, so each 16-byte load instruction of a warp reads four whole 128-byte lines
+// (four lanes per block, each reading 64 contiguous bytes, measured twice as slow: every load
+// instruction then touches sixteen half-used lines).  Each group keeps kQUnroll blocks in flight.
+// The (row, K block) of an item advances by fixed steps: no integer division in the loop.
+constexpr int kQThreads = 128;
+constexpr int kQUnroll = 4;
+constexpr int kQLanes = 8;  // lanes per block
+constexpr int kQGroupsPerBlock = kQThreads / kQLanes;
+// Grids of the 1x128 quantiser are capped at the blocks that are resident at once (the occupancy
+// of the instantiation, looked up once per device): a grid larger than one wave would leave a
+// partial last wave, measured 5-20% slower on the bench activations.
+
+// (row, K block) of item i = row * KB + kb
+struct RowKb {
+  uint32_t m, kb;
+};
+__device__ __forceinline__ void advance(RowKb& p, uint32_t dm, uint32_t dkb, uint32_t KB) {
+  p.m += dm;
+  p.kb += dkb;
+  if (p.kb >= KB) {
+    p.kb -= KB;
+    ++p.m;
+  }
+}
 
 // GATHER: output row m holds input row row_src[m] (a zero row where row_src[m] < 0).
 // FMT: e4m3 (s = amax / 448) or e5m2 (gradients, s = amax / 57344).
@@ -174,9 +216,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa,
     const int32_t* __restrict__ row_src, uint32_t cap = 0) {
-  const int sub = threadIdx.x & 7;
-  const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) >> 3;
-  const uint32_t n_groups = gridDim.x * (kQThreads >> 3);
+  const int sub = threadIdx.x & (kQLanes - 1);
+  const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) / kQLanes;
+  const uint32_t n_groups = gridDim.x * kQGroupsPerBlock;
   uint32_t total = M * KB;  // the host guarantees M * KB < 2^31
   uint32_t row0 = 0;        // MASKED: the expert's first row
   if (MASKED) {
@@ -184,22 +226,28 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     total = static_cast<uint32_t>(min(max(cnt, 0), static_cast<int32_t>(cap))) * KB;
     row0 = blockIdx.y * cap;
   }
-  for (uint32_t base = group; base - group < total; base += n_groups * kQUnroll) {
+  // steps between this group's items: n_groups within a pass, n_groups * kQUnroll between passes
+  const uint32_t step_m = n_groups / KB, step_kb = n_groups - step_m * KB;
+  const uint32_t pass = n_groups * kQUnroll;
+  const uint32_t pass_m = pass / KB, pass_kb = pass - pass_m * KB;
+  RowKb p{group / KB, group - (group / KB) * KB};
+  for (uint32_t base = group; base < total; base += pass, advance(p, pass_m, pass_kb, KB)) {
     uint4 raw[kQUnroll][2];
-    uint32_t m[kQUnroll], kb[kQUnroll];
+    RowKb it[kQUnroll];
     bool live[kQUnroll];
 #pragma unroll
     for (int u = 0; u < kQUnroll; ++u) {
-      const uint32_t item = base + u * n_groups;
-      m[u] = item / KB;
-      kb[u] = item - m[u] * KB;
-      m[u] += row0;
+      it[u] = p;
+      if (u > 0) {
+        it[u] = it[u - 1];
+        advance(it[u], step_m, step_kb, KB);
+      }
+      live[u] = base + u * n_groups < total;
       raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
-      live[u] = item < total;
-      int64_t src_row = m[u];
-      if (GATHER && live[u]) src_row = __ldg(row_src + m[u]);
+      int64_t src_row = it[u].m + row0;
+      if (GATHER && live[u]) src_row = __ldg(row_src + it[u].m);
       if (live[u] && src_row >= 0) {
-        const __nv_bfloat16* src = x + src_row * ldx + kb[u] * 128 + sub * 8;
+        const __nv_bfloat16* src = x + src_row * ldx + it[u].kb * 128 + sub * 8;
         raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
         raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 64));
       }
@@ -218,14 +266,15 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
       // reduce over the 8 lanes of this group (xor offsets < 8 stay inside it)
 #pragma unroll
       for (int off = 4; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-      const float s = __fdiv_rn(a, FMT == kE5M2 ? kE5M2Max : kE4M3Max);
+      const float s = block_scale<FMT>(a);
       if (live[u]) {
         uint32_t c[4];
         quant_n<16, FMT>(f, s, FMT == kE4M3 ? direct_mode(a, s) : 0u, c);
-        uint8_t* dst = q + m[u] * ldq + kb[u] * 128 + sub * 8;
+        const uint32_t m = it[u].m + row0;
+        uint8_t* dst = q + static_cast<int64_t>(m) * ldq + it[u].kb * 128 + sub * 8;
         *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
         *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
-        if (sub == 0) sA[kb[u] * ld_sa + m[u]] = s;
+        if (sub == 0) sA[static_cast<int64_t>(it[u].kb) * ld_sa + m] = s;
       }
     }
   }
@@ -560,6 +609,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
   if (tid == 0 && (s_bad || !fits)) record_status(status, FP8G_ERR_DEVICE_ASSERT);
 }
 
+// Resident blocks of `kern` (kQThreads threads, no dynamic shared memory) across the device.
+template <typename Kernel>
+int64_t resident_blocks(Kernel kern, const DeviceInfo* dev) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQThreads, 0) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  return static_cast<int64_t>(per_sm) * dev->sm_count;
+}
+
 }  // namespace
 }  // namespace fp8g
 
@@ -579,9 +639,9 @@ extern "C" int fp8_quantize_1x128(const void* x, int64_t M, int64_t K, int64_t l
   if (st != FP8G_OK) return st;
   const int64_t items = M * (K / 128);
   if (items >= (int64_t{1} << 31) || M > 0x7FFFFFFF) return FP8G_ERR_INVALID_ARG;
-  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  const int64_t per_block = kQGroupsPerBlock * kQUnroll;
   int64_t blocks = (items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
+  static const int64_t cap = resident_blocks(quantize_1x128_kernel<false>, dev);
   if (blocks > cap) blocks = cap;
   quantize_1x128_kernel<false><<<static_cast<unsigned>(blocks), kQThreads, 0,
                                  static_cast<cudaStream_t>(stream)>>>(
@@ -608,9 +668,10 @@ extern "C" int fp8_quantize_1x128_masked(const void* x, int32_t E, int64_t cap, 
   const int64_t items = M * (K / 128);
   if (items >= (int64_t{1} << 31) || E > 65535) return FP8G_ERR_INVALID_ARG;
   // one grid row per expert, sized for a full expert; CTAs past an expert's count exit at once
-  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  const int64_t per_block = kQGroupsPerBlock * kQUnroll;
   int64_t bx = (cap * (K / 128) + per_block - 1) / per_block;
-  const int64_t limit = std::max<int64_t>(1, static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads) / E);
+  static const int64_t resident = resident_blocks(quantize_1x128_kernel<false, kE4M3, true>, dev);
+  const int64_t limit = std::max<int64_t>(1, resident / E);
   if (bx > limit) bx = limit;
   const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(E));
   quantize_1x128_kernel<false, kE4M3, true><<<grid, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
@@ -633,9 +694,9 @@ extern "C" int fp8_quantize_1x128_e5m2(const void* x, int64_t M, int64_t K, int6
   if (st != FP8G_OK) return st;
   const int64_t items = M * (K / 128);
   if (items >= (int64_t{1} << 31) || M > 0x7FFFFFFF) return FP8G_ERR_INVALID_ARG;
-  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  const int64_t per_block = kQGroupsPerBlock * kQUnroll;
   int64_t blocks = (items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
+  static const int64_t cap = resident_blocks(quantize_1x128_kernel<false, kE5M2>, dev);
   if (blocks > cap) blocks = cap;
   quantize_1x128_kernel<false, kE5M2><<<static_cast<unsigned>(blocks), kQThreads, 0,
                                         static_cast<cudaStream_t>(stream)>>>(
@@ -674,9 +735,9 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
                                                     row_token, M_cap, dev->status);
   if (cudaGetLastError() != cudaSuccess) return FP8G_ERR_CUDA;
   const int64_t items = M_cap * (K / 128);
-  const int64_t per_block = (kQThreads / 8) * kQUnroll;
+  const int64_t per_block = kQGroupsPerBlock * kQUnroll;
   int64_t blocks = (items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(dev->sm_count) * (2048 / kQThreads);
+  static const int64_t cap = resident_blocks(quantize_1x128_kernel<true>, dev);
   if (blocks > cap) blocks = cap;
   quantize_1x128_kernel<true><<<static_cast<unsigned>(blocks), kQThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M_cap), static_cast<uint32_t>(K / 128), ldx,
