@@ -380,6 +380,7 @@ def run_ours(args, world, rank, local, dist):
     roof["traffic"] = traffic_for(key)
     roof["share"] = round(top[1] / sum(k[1] for k in kernels), 3)
 
+    breakdown["tiny"] = measure_tiny_latency(g, dev, fp8_peak)
     e2e = measure_e2e(cases, g, dev, max(3, min(args.steps, 20)), dist, world)
     next_rows = measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak)
     library = measure_library_rows(cases, flush, fp8_peak, breakdown)
@@ -407,6 +408,62 @@ def run_ours(args, world, rank, local, dist):
         out["cpu_baseline"] = cpu_baseline(names, target_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def measure_tiny_latency(g, dev, fp8_peak, reps=200):
+    """The tiny dense configuration (M=128, N=256, K=512) as a latency row, beside the headline
+    step (not part of it): quantise A (1x128) and the GEMM, each launched `reps` times back to back
+    between two CUDA events, and the pair together; microseconds per launch.  Its inputs stay in L2."""
+    c = Case("tiny", g, dev)
+    stream = torch.cuda.current_stream()
+
+    def per_call(fn):
+        for _ in range(5):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def in_graph(fn, n=50):
+        # device time per launch: n launches captured once in a CUDA graph, the graph replayed
+        fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(n):
+                fn()
+        for _ in range(3):
+            graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(10):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (10 * n)
+
+    q_us = per_call(c.quantize)
+    g_us = per_call(c.gemm)
+    pair_us = per_call(lambda: (c.quantize(), c.gemm()))
+    q_dev, g_dev = in_graph(c.quantize), in_graph(c.gemm)
+    pair_dev = in_graph(lambda: (c.quantize(), c.gemm()))
+    if g.fp8g_get_status() != 0:
+        raise RuntimeError("device status not OK after the tiny latency row")
+    tf = c.flops / (g_dev * 1e-6) / 1e12
+    return {"latency_row": "measured on its own; not in the headline step",
+            "shape": "M=128, N=256, K=512",
+            "device_us": {"quant": round(q_dev, 2), "gemm": round(g_dev, 2), "quant_plus_gemm": round(pair_dev, 2),
+                          "how": "launches captured in a CUDA graph and replayed back to back"},
+            "api_call_us": {"quant": round(q_us, 2), "gemm": round(g_us, 2), "quant_plus_gemm": round(pair_us, 2),
+                            "how": "Python binding calls back to back (host-bound: argument checks, tensor maps, launch)"},
+            "gemm_us": round(g_dev, 2), "quant_us": round(q_dev, 2),
+            "gemm_tflops": round(tf, 2), "pct_fp8_peak": round(100 * tf / fp8_peak, 2), "launches": 2}
 
 
 def _time_calls(call, flush, reps=20, warm=3):

@@ -174,6 +174,11 @@ struct GemmArgs {
   int32_t sk_min_gain;  // split only when it saves at least this many K blocks per CTA
   float4* ws_part;
   uint32_t* ws_flag;
+
+  // Test hook, -1 normally: the producer never fills its stage number `test_skip_stage` (counted
+  // over the CTA's stages), so the MMA issuer's bounded wait for it runs out and the abort path
+  // runs (FP8G_ERR_TIMEOUT; every role leaves, in-flight copies and MMAs are awaited, TMEM freed).
+  int32_t test_skip_stage;
 };
 
 struct Tile {
@@ -628,6 +633,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
         if (!fetch_tile(pc, ti)) continue;
         // the K blocks of a stage past the end of K are zero-filled and never read
         for (int32_t kb = pc.kb0; kb < pc.kb1; kb += KPS, ++it) {
+          if (static_cast<int32_t>(it) == a.test_skip_stage) continue;  // test hook (see GemmArgs)
           const uint32_t s = it % S, ph = (it / S) & 1u;
           bool ready;
           if constexpr (kLone) {
@@ -1271,6 +1277,13 @@ bool sk_workspace(int dev, int sm_count, cudaStream_t stream, float4** part, uin
   return true;
 }
 
+// FP8G_TEST_SKIP_STAGE=<n> (tests only, read on every call): the producer of every CTA leaves its
+// stage n unfilled, so the issuer's wait for it runs out (see GemmArgs::test_skip_stage).
+int env_test_skip_stage() {
+  const char* e = std::getenv("FP8G_TEST_SKIP_STAGE");
+  return e ? std::atoi(e) : -1;
+}
+
 // FP8G_STREAMK=0 turns the stream-K tail off (read on every call).
 bool env_streamk() {
   const char* e = std::getenv("FP8G_STREAMK");
@@ -1374,6 +1387,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   a.sb_step = o.sb_step;
   a.idesc_fmt = o.idesc_fmt;
   a.ld_sb = o.ld_sb;
+  a.test_skip_stage = env_test_skip_stage();
   if (MODE == kKGrouped) a.num_tiles = static_cast<int32_t>(o.E) * a.num_m * a.num_n;
 
   // K blocks per stage of the variant launched below (its Cfg::kKPS)
