@@ -62,7 +62,7 @@ enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3, kK
 
 constexpr int BM = 128;  // rows per tile = TMEM lanes
 constexpr int BK = 128;  // K per stage = the scaling block
-constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a band)
+constexpr int kBandM = 16;  // m-blocks per raster band of CTA pairs (L2 reuse of B across a band)
 
 // PAIR: a cluster of two CTAs computes 256 x BN tiles with tcgen05.mma.cta_group::2; each CTA
 // loads its 128 A rows and half of the B tile (BN / 2 rows), so a stage is 32 KB and six fit.
@@ -72,9 +72,11 @@ constexpr int kBandM = 16;  // m-blocks per raster band (L2 reuse of B across a 
 // warp's 512 bytes of per-column B scales.
 template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
 struct Cfg {
-  // columns per epilogue warp.  256 x 128 pair tiles: 64, so that each warp reads its whole
-  // partial with one load and frees the TMEM buffer before any FMA.
-  static constexpr int kEpiCols = (PAIR && BN == 128) ? 64 : (BN >= 128 ? 128 : BN);
+  // columns per epilogue warp.  192-wide tiles and 256 x 128 pair tiles: 64, so that each warp
+  // reads its whole partial with one load and frees the TMEM buffer before any FMA (a 128-column
+  // warp holds 128 accumulators and can load only half its partial at a time, so the FMAs of the
+  // first half sit between the buffer's completion and its release).
+  static constexpr int kEpiCols = ((PAIR && BN == 128) || BN == 192) ? 64 : (BN >= 128 ? 128 : BN);
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
   // Narrow tiles (few, long K loops: small-M shapes) split the K blocks between two sets of
   // promotion warps (even / odd K blocks), whose FP32 partial sums are added at the tile end.
@@ -88,14 +90,16 @@ struct Cfg {
   // Wider tiles keep one: their MMAs are long enough, and measured slower with two.
   // 256 x 128 pair tiles: four MMAs of ~64 cycles per K block for the pair, so two lone issuers.
   static constexpr int kMmaWarps = (SMALL || (PAIR && BN == 128)) ? 2 : 1;
-  // BN = 256: three full warpgroups (producer / 2 MMA / idle, then 2 epilogue warpgroups) so
-  // that setmaxnreg can move registers to the epilogue: the launch gives 384 x 168 = 64512,
-  // rebalanced to 128 x 40 + 256 x 232 = 64512.  Otherwise: producer and MMA warps, then the
-  // epilogue warpgroups (any four consecutive warps cover the four TMEM lane quarters).
-  static constexpr int kEpiWarp0 = BN == 256 ? 4 : 1 + kMmaWarps;
+  // BN = 256 and 192: a full first warpgroup (producer / MMA / idle) then the epilogue
+  // warpgroups, so that setmaxnreg can move registers to the epilogue.  BN = 256: the launch gives
+  // 384 x 168 = 64512, rebalanced to 128 x 40 + 256 x 232 = 64512.  BN = 192: 512 x 128 = 65536,
+  // rebalanced to 128 x 32 + 384 x 160 = 65536 (64 accumulators and 64 loaded values a thread).
+  // Otherwise: producer and MMA warps, then the epilogue warpgroups (any four consecutive warps
+  // cover the four TMEM lane quarters).
+  static constexpr bool kRebalance = BN == 256 || BN == 192;
+  static constexpr int kEpiWarp0 = kRebalance ? 4 : 1 + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
-  static constexpr bool kRebalance = BN == 256;
-  static constexpr uint32_t kRegsLow = 40, kRegsHigh = 232;
+  static constexpr uint32_t kRegsLow = BN == 192 ? 32 : 40, kRegsHigh = BN == 192 ? 160 : 232;
   // A rows loaded per stage: the MMA always reads 128 rows, and with SMALL the upper 64 are
   // whatever follows in shared memory (those rows of D are computed but never stored).
   static constexpr int kARows = SMALL ? 64 : BM;
@@ -104,7 +108,7 @@ struct Cfg {
   // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
   static constexpr int kKPS = SMALL ? 2 : 1;
   static constexpr int kStages =
-      SMALL ? 6 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN == 256 ? 4 : 6)));
+      SMALL ? 6 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : 6)));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
@@ -140,7 +144,8 @@ struct Cfg {
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
   static_assert(kOffScale % 128 == 0 && kScaleStage % 128 == 0 && kOffSbv % 16 == 0, "scale staging alignment");
-  static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+  static_assert(BN == 64 || BN == 128 || BN == 192 || BN == 256, "BN");
+  static_assert(BN != 192 || (!SMALL && !PAIR && !KG), "192-wide tiles: single-CTA block-scaled forms");
   static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
   static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
@@ -152,6 +157,7 @@ struct GemmArgs {
   int32_t num_m;     // m-blocks (dense / contiguous)
   int32_t num_n;     // n-blocks of BN
   int32_t num_tiles; // dense / contiguous tile count
+  int32_t band_m;    // m-blocks per raster band (dense / contiguous / K-grouped; see band_rows)
   const float* sA;   // A-row scales [KB][ld_sa]
   int64_t ld_sa;
   const float* sB;
@@ -287,10 +293,10 @@ __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table
     // expert e = t / (m-blocks x n-blocks), then the dense banded raster within the expert
     const int32_t per_e = a.num_m * a.num_n;
     const int32_t e = t / per_e, r = t - e * per_e;
-    const int32_t band_tiles = kBandM * a.num_n;
+    const int32_t band_tiles = a.band_m * a.num_n;
     const int32_t band = r / band_tiles, rr = r - band * band_tiles;
-    const int32_t m_first = band * kBandM;
-    const int32_t gm = min(kBandM, a.num_m - m_first);
+    const int32_t m_first = band * a.band_m;
+    const int32_t gm = min(a.band_m, a.num_m - m_first);
     const int32_t mb = m_first + rr % gm, nb = rr / gm;
     ti.g = e;
     ti.a_row = mb * BM;
@@ -322,10 +328,10 @@ __device__ __forceinline__ bool get_tile(const GemmArgs& a, const int32_t* table
     ti.rows = min(BM, cnt - mb * BM);
     return ti.rows > 0;
   } else {
-    const int32_t band_tiles = kBandM * a.num_n;
+    const int32_t band_tiles = a.band_m * a.num_n;
     const int32_t band = t / band_tiles, r = t - band * band_tiles;
-    const int32_t m_first = band * kBandM;
-    const int32_t gm = min(kBandM, a.num_m - m_first);
+    const int32_t m_first = band * a.band_m;
+    const int32_t gm = min(a.band_m, a.num_m - m_first);
     const int32_t mb = m_first + r % gm, nb = r / gm;
     ti.a_row = mb * BM;
     ti.d_row = ti.a_row;
@@ -1156,6 +1162,7 @@ constexpr int kMaxExperts = 2048;
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB: the per-block dynamic shared memory limit
 static_assert(Cfg<256>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+static_assert(Cfg<192>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
@@ -1188,7 +1195,7 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
         return FP8G_ERR_CUDA;
       }
       if (fa.numRegs * C::kThreads < 128 * static_cast<int>(C::kRegsLow) +
-                                         256 * static_cast<int>(C::kRegsHigh))
+                                         (C::kThreads - 128) * static_cast<int>(C::kRegsHigh))
         return FP8G_ERR_CUDA;
     }
     attr_set.fetch_or(bit);
@@ -1284,6 +1291,21 @@ int env_test_skip_stage() {
   return e ? std::atoi(e) : -1;
 }
 
+// Raster band height (m-blocks).  Tiles run m-block fastest within a band of m-blocks and n-block
+// by n-block, so the CTAs in flight share the band's A rows and a few B column blocks in L2.  When
+// all of A fits well inside L2 (<= 48 MB) the band is all of M: each B column block is then read
+// from DRAM once, with A staying resident; otherwise 16 m-blocks (2048 rows), whose A slab stays
+// resident while B streams once per band.  FP8G_BAND_M overrides (read on every call).
+int32_t band_rows(int32_t num_m, int64_t K, bool kgrouped) {
+  if (const char* e = std::getenv("FP8G_BAND_M")) {
+    const int v = std::atoi(e);
+    if (v > 0) return v;
+  }
+  if (kgrouped) return kBandM;
+  const int64_t a_bytes = static_cast<int64_t>(num_m) * BM * K;
+  return a_bytes <= (int64_t{48} << 20) ? (num_m > 0 ? num_m : 1) : kBandM;
+}
+
 // FP8G_STREAMK=0 turns the stream-K tail off (read on every call).
 bool env_streamk() {
   const char* e = std::getenv("FP8G_STREAMK");
@@ -1300,11 +1322,11 @@ int env_pair() {
   return (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) ? e[0] - '0' : 0;
 }
 
-// FP8G_BLOCK_N (64, 128 or 256) forces the tile width; read on every call.
+// FP8G_BLOCK_N (64, 128, 192 or 256) forces the tile width; read on every call.
 int env_block_n() {
   const char* e = std::getenv("FP8G_BLOCK_N");
   const int x = e ? std::atoi(e) : 0;
-  return (x == 64 || x == 128 || x == 256) ? x : 0;
+  return (x == 64 || x == 128 || x == 192 || x == 256) ? x : 0;
 }
 
 // Pick BN: fewest (waves x per-tile cost), the per-tile cost growing with BN plus a fixed
@@ -1356,6 +1378,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
                            : (MODE == kKGrouped) ? o.E * ((o.rows + BM - 1) / BM)
                                                  : (o.rows + BM - 1) / BM;
   int bn = choose_block_n(m_blocks, o.N, dev->sm_count, (EPI || MODE == kKGrouped) ? 128 : 64);
+  if ((EPI || MODE == kKGrouped) && bn == 192) bn = 256;  // those forms have 128- and 256-wide tiles
   // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
   const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
@@ -1388,6 +1411,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   a.idesc_fmt = o.idesc_fmt;
   a.ld_sb = o.ld_sb;
   a.test_skip_stage = env_test_skip_stage();
+  a.band_m = band_rows(a.num_m, o.K, MODE == kKGrouped);
   if (MODE == kKGrouped) a.num_tiles = static_cast<int32_t>(o.E) * a.num_m * a.num_n;
 
   // K blocks per stage of the variant launched below (its Cfg::kKPS)
@@ -1521,6 +1545,9 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
         }
         t_last_stages = Cfg<256>::kStages;
         return launch_kernel<256, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
+      case 192:
+        t_last_stages = Cfg<192>::kStages;
+        return launch_kernel<192, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
       case 128:
         if (pair) {
           t_last_stages = Cfg<128, false, true>::kStages;
