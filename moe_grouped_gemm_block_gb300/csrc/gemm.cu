@@ -72,11 +72,12 @@ constexpr int kBandM = 16;  // m-blocks per raster band of CTA pairs (L2 reuse o
 // warp's 512 bytes of per-column B scales.
 template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
 struct Cfg {
-  // columns per epilogue warp.  192-wide tiles and 256 x 128 pair tiles: 64, so that each warp
-  // reads its whole partial with one load and frees the TMEM buffer before any FMA (a 128-column
-  // warp holds 128 accumulators and can load only half its partial at a time, so the FMAs of the
-  // first half sit between the buffer's completion and its release).
-  static constexpr int kEpiCols = ((PAIR && BN == 128) || BN == 192) ? 64 : (BN >= 128 ? 128 : BN);
+  // columns per epilogue warp.  192-wide tiles and 256 x 128 pair tiles: 64, 160-wide tiles: 32,
+  // so that each warp reads its whole partial with one load and frees the TMEM buffer before any
+  // FMA (a 128-column warp holds 128 accumulators and can load only half its partial at a time, so
+  // the FMAs of the first half sit between the buffer's completion and its release).
+  static constexpr int kEpiCols =
+      BN == 160 ? 32 : (((PAIR && BN == 128) || BN == 192) ? 64 : (BN >= 128 ? 128 : BN));
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
   // Narrow tiles (few, long K loops: small-M shapes) split the K blocks between two sets of
   // promotion warps (even / odd K blocks), whose FP32 partial sums are added at the tile end.
@@ -88,18 +89,21 @@ struct Cfg {
   // One thread pays ~60 cycles per tcgen05.mma plus ~170 per mbarrier round trip, which caps
   // the narrow small-M tiles (whose MMAs are short); there two issuers share the stream.
   // Wider tiles keep one: their MMAs are long enough, and measured slower with two.
-  // 256 x 128 pair tiles: four MMAs of ~64 cycles per K block for the pair, so two lone issuers.
-  static constexpr int kMmaWarps = (SMALL || (PAIR && BN == 128)) ? 2 : 1;
-  // BN = 256 and 192: a full first warpgroup (producer / MMA / idle) then the epilogue
+  // 256 x 128 pair tiles: four MMAs of ~64 cycles per K block for the pair, so two lone issuers;
+  // 160-wide tiles: four MMAs of ~81 cycles per K block, also two.
+  static constexpr int kMmaWarps = (SMALL || (PAIR && BN == 128) || BN == 160) ? 2 : 1;
+  // BN = 256, 192 and 160: a full first warpgroup (producer / MMA / idle) then the epilogue
   // warpgroups, so that setmaxnreg can move registers to the epilogue.  BN = 256: the launch gives
   // 384 x 168 = 64512, rebalanced to 128 x 40 + 256 x 232 = 64512.  BN = 192: 512 x 128 = 65536,
   // rebalanced to 128 x 32 + 384 x 160 = 65536 (64 accumulators and 64 loaded values a thread).
-  // Otherwise: producer and MMA warps, then the epilogue warpgroups (any four consecutive warps
-  // cover the four TMEM lane quarters).
-  static constexpr bool kRebalance = BN == 256 || BN == 192;
+  // BN = 160: 768 x 80 = 61440, rebalanced to 128 x 40 + 640 x 88 = 61440 (32 accumulators and 32
+  // loaded values).  Otherwise: producer and MMA warps, then the epilogue warpgroups (any four
+  // consecutive warps cover the four TMEM lane quarters).
+  static constexpr bool kRebalance = BN == 256 || BN == 192 || BN == 160;
   static constexpr int kEpiWarp0 = kRebalance ? 4 : 1 + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
-  static constexpr uint32_t kRegsLow = BN == 192 ? 32 : 40, kRegsHigh = BN == 192 ? 160 : 232;
+  static constexpr uint32_t kRegsLow = BN == 192 ? 32 : 40;
+  static constexpr uint32_t kRegsHigh = BN == 256 ? 232 : (BN == 192 ? 160 : 88);
   // A rows loaded per stage: the MMA always reads 128 rows, and with SMALL the upper 64 are
   // whatever follows in shared memory (those rows of D are computed but never stored).
   static constexpr int kARows = SMALL ? 64 : BM;
@@ -108,9 +112,9 @@ struct Cfg {
   // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
   static constexpr int kKPS = SMALL ? 2 : 1;
   static constexpr int kStages =
-      SMALL ? 6 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : 6)));
+      SMALL ? 6 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 5 : 6))));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
-  // promotion by several K blocks (2 at BN = 256, 4 at 128, 8 at 64).
+  // promotion by several K blocks (2 at BN = 256, 3 at 160, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kABytes = kARows * BK;       // one K block of A
@@ -144,8 +148,9 @@ struct Cfg {
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
   static_assert(kOffScale % 128 == 0 && kScaleStage % 128 == 0 && kOffSbv % 16 == 0, "scale staging alignment");
-  static_assert(BN == 64 || BN == 128 || BN == 192 || BN == 256, "BN");
-  static_assert(BN != 192 || (!SMALL && !PAIR && !KG), "192-wide tiles: single-CTA block-scaled forms");
+  static_assert(BN == 64 || BN == 128 || BN == 160 || BN == 192 || BN == 256, "BN");
+  static_assert((BN != 192 && BN != 160) || (!SMALL && !PAIR && !KG),
+                "160- and 192-wide tiles: single-CTA block-scaled forms");
   static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
   static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
@@ -401,6 +406,10 @@ __device__ __forceinline__ void get_pair_tile(const GemmArgs& a, const int32_t* 
   }
   ti.d_row = ti.a_row;
 }
+
+// One TMEM load of 32 or 64 columns with its wait (tcgen05.ld 32x32b.x32 / .x64).
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[32]) { tmem_ld32_sync(taddr, v); }
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[64]) { tmem_ld64_sync(taddr, v); }
 
 // Bounded wait on an mbarrier phase.  On timeout: flag the CTA, record the status.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmArgs& a,
@@ -937,16 +946,19 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
           if (live) {
+            // this warp's columns in loads of kLd (one load and its wait each)
+            constexpr int kLd = C::kEpiCols >= 64 ? 64 : C::kEpiCols;
 #pragma unroll
-            for (int c = 0; c < C::kEpiCols / 64; ++c) {
-              float v[64];
-              tmem_ld64_sync(taddr + c * 64, v);
-              if (c == C::kEpiCols / 64 - 1) {  // all of this warp's columns are in registers:
-                tc_fence_before();               // release the TMEM buffer before the last FMAs
+            for (int c = 0; c < C::kEpiCols / kLd; ++c) {
+              float v[kLd];
+              tmem_ld_sync(taddr + c * kLd, v);
+              if (c == C::kEpiCols / kLd - 1) {  // all of this warp's columns are in registers:
+                tc_fence_before();                // release the TMEM buffer before the last FMAs
                 __syncwarp();
                 release_tmem(b);
               }
               if constexpr (MODE == kKGrouped) {
+                static_assert(MODE != kKGrouped || kLd == 64, "K-grouped tiles load 64 columns at a time");
                 // one B scale per column: s[n] = sa * sB[kb][n]
                 const float2 sa2 = make_float2(sa_kb, sa_kb);
 #pragma unroll
@@ -960,8 +972,9 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
                 }
               } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  acc[c * 32 + i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * 32 + i]);
+                for (int i = 0; i < kLd / 2; ++i)
+                  acc[c * (kLd / 2) + i] =
+                      __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), scale2, acc[c * (kLd / 2) + i]);
               }
             }
           } else {
@@ -1163,6 +1176,10 @@ constexpr uint32_t kSmemLimit = 232448;  // 227 KB: the per-block dynamic shared
 static_assert(Cfg<256>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<192>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
+// 160-wide tiles (five 36 KB stages and twenty 2 KB staging boxes) leave room for the group tables
+// of up to 512 experts; grouped calls with more experts take 256-wide tiles.
+constexpr int kMaxExperts160 = 512;
+static_assert(Cfg<160>::kOffTable + 4 * (kMaxExperts160 + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
@@ -1292,16 +1309,23 @@ int env_test_skip_stage() {
 }
 
 // Raster band height (m-blocks).  Tiles run m-block fastest within a band of m-blocks and n-block
-// by n-block, so the CTAs in flight share the band's A rows and a few B column blocks in L2.  When
-// all of A fits well inside L2 (<= 48 MB) the band is all of M: each B column block is then read
-// from DRAM once, with A staying resident; otherwise 16 m-blocks (2048 rows), whose A slab stays
-// resident while B streams once per band.  FP8G_BAND_M overrides (read on every call).
-int32_t band_rows(int32_t num_m, int64_t K, bool kgrouped) {
+// by n-block, so the CTAs in flight share the band's A rows and a few B column blocks in L2.
+//   Dense: when all of A fits well inside L2 (<= 48 MB) the band is all of M, so each B column
+//   block is read from DRAM once with A staying resident (4096 x 8192 x 8192: 220 us against 226
+//   with 16 m-blocks); otherwise 16 m-blocks (2048 rows), whose A slab stays resident while B
+//   streams once per band.
+//   Contiguous-grouped: 8 m-blocks.  A band spanning every expert keeps all experts' B column blocks
+//   in flight at once (the grouped data gradient, 8576 x 7168 x 4096: 248 us with all 67 m-blocks,
+//   226 us with 8 or 16; the MoE forward GEMM: 231 us with 8, 236 us with 16).
+//   K-grouped: 16.
+// FP8G_BAND_M overrides (read on every call).
+int32_t band_rows(int32_t num_m, int64_t K, int mode) {
   if (const char* e = std::getenv("FP8G_BAND_M")) {
     const int v = std::atoi(e);
     if (v > 0) return v;
   }
-  if (kgrouped) return kBandM;
+  if (mode == kContiguous) return 8;
+  if (mode != kDense) return kBandM;
   const int64_t a_bytes = static_cast<int64_t>(num_m) * BM * K;
   return a_bytes <= (int64_t{48} << 20) ? (num_m > 0 ? num_m : 1) : kBandM;
 }
@@ -1322,11 +1346,15 @@ int env_pair() {
   return (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) ? e[0] - '0' : 0;
 }
 
-// FP8G_BLOCK_N (64, 128, 192 or 256) forces the tile width; read on every call.
+// FP8G_BLOCK_N (64, 128, 160, 192 or 256) forces the tile width; read on every call.  160 and 192
+// are only taken this way: measured slower than 256 on the large shapes (4096 x 8192 x 8192: 361 and
+// 288 us against 212).  Per K block a narrower tile still needs four tcgen05.mma, and one issuing
+// thread took ~620 cycles for the four N = 160 MMAs and their commit against ~325 cycles of MMA
+// work (a second issuer measured the same), so those tiles are issue-bound.
 int env_block_n() {
   const char* e = std::getenv("FP8G_BLOCK_N");
   const int x = e ? std::atoi(e) : 0;
-  return (x == 64 || x == 128 || x == 192 || x == 256) ? x : 0;
+  return (x == 64 || x == 128 || x == 160 || x == 192 || x == 256) ? x : 0;
 }
 
 // Pick BN: fewest (waves x per-tile cost), the per-tile cost growing with BN plus a fixed
@@ -1378,7 +1406,8 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
                            : (MODE == kKGrouped) ? o.E * ((o.rows + BM - 1) / BM)
                                                  : (o.rows + BM - 1) / BM;
   int bn = choose_block_n(m_blocks, o.N, dev->sm_count, (EPI || MODE == kKGrouped) ? 128 : 64);
-  if ((EPI || MODE == kKGrouped) && bn == 192) bn = 256;  // those forms have 128- and 256-wide tiles
+  if ((EPI || MODE == kKGrouped) && (bn == 192 || bn == 160)) bn = 256;  // those forms: 128 and 256 wide
+  if (bn == 160 && MODE != kDense && o.E > kMaxExperts160) bn = 256;    // group table too large
   // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
   const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
@@ -1411,7 +1440,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   a.idesc_fmt = o.idesc_fmt;
   a.ld_sb = o.ld_sb;
   a.test_skip_stage = env_test_skip_stage();
-  a.band_m = band_rows(a.num_m, o.K, MODE == kKGrouped);
+  a.band_m = band_rows(a.num_m, o.K, MODE == kDenseSmallM ? kDense : MODE);
   if (MODE == kKGrouped) a.num_tiles = static_cast<int32_t>(o.E) * a.num_m * a.num_n;
 
   // K blocks per stage of the variant launched below (its Cfg::kKPS)
@@ -1486,7 +1515,8 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
     if (u < umin) u = umin;
     return U > 0 && KB - u >= a.sk_min_gain;
   };
-  if (MODE != kKGrouped && !pair && !small_m && bn >= 128 && env_streamk() &&
+  // (160-wide tiles have two MMA issuers, which take whole tiles)
+  if (MODE != kKGrouped && !pair && !small_m && bn >= 128 && bn != 160 && env_streamk() &&
       (MODE == kMasked || tail_splits(a.num_tiles))) {
     int dev_id = 0;
     cudaGetDevice(&dev_id);
@@ -1548,6 +1578,9 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
       case 192:
         t_last_stages = Cfg<192>::kStages;
         return launch_kernel<192, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
+      case 160:
+        t_last_stages = Cfg<160>::kStages;
+        return launch_kernel<160, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
       case 128:
         if (pair) {
           t_last_stages = Cfg<128, false, true>::kStages;

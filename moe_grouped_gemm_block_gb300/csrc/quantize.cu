@@ -667,11 +667,15 @@ extern "C" int fp8_quantize_1x128_masked(const void* x, int32_t E, int64_t cap, 
   const int64_t M = static_cast<int64_t>(E) * cap;
   const int64_t items = M * (K / 128);
   if (items >= (int64_t{1} << 31) || E > 65535) return FP8G_ERR_INVALID_ARG;
-  // one grid row per expert, sized for a full expert; CTAs past an expert's count exit at once
+  // one grid row per expert, sized for a full expert; CTAs past an expert's count exit at once.
+  // Capped at twice the resident blocks over all experts: the counts differ between experts, so
+  // one wave's worth (each expert's blocks striding over its rows) leaves the fullest experts
+  // last (MoE masked activations, 32 experts x 256 rows x 7168: 37.5 us at one wave, 33.4 us at
+  // two or uncapped).
   const int64_t per_block = kQGroupsPerBlock * kQUnroll;
   int64_t bx = (cap * (K / 128) + per_block - 1) / per_block;
   static const int64_t resident = resident_blocks(quantize_1x128_kernel<false, kE4M3, true>, dev);
-  const int64_t limit = std::max<int64_t>(1, resident / E);
+  const int64_t limit = std::max<int64_t>(1, 2 * resident / E);
   if (bx > limit) bx = limit;
   const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(E));
   quantize_1x128_kernel<false, kE4M3, true><<<grid, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(

@@ -54,6 +54,7 @@ def _dense_gpu(qa, sa, qb, sb, bn=None):
     (128, 256, 512, None), (1, 16, 128, 64), (64, 64, 128, None), (200, 208, 384, 256),
     (200, 208, 384, 128), (200, 208, 384, 64), (300, 512, 1024, 256), (129, 272, 256, 128),
     (200, 208, 384, 192), (300, 592, 1024, 192), (513, 400, 640, 192),
+    (200, 208, 384, 160), (300, 592, 1024, 160), (513, 400, 640, 160), (257, 1024, 640, 160),
     (64, 1792, 7168, 64), (257, 1024, 640, 256), (513, 384, 256, None),
     (40, 256, 384, 64), (17, 128, 1152, 64),  # small M, odd K-block counts (part-filled stages)
 ])
@@ -135,7 +136,8 @@ def _contig_gpu(qa, sa, qb, sb, offs, bn=None):
     return D
 
 
-@pytest.mark.parametrize("bn,use_pair", [(None, 1), (256, 1), (256, 0), (192, 0), (128, 1), (64, 1), (None, 2), (256, 2)])
+@pytest.mark.parametrize("bn,use_pair", [(None, 1), (256, 1), (256, 0), (192, 0), (160, 0), (128, 1), (64, 1), (None, 2),
+                                          (256, 2)])
 def test_contiguous_small(bn, use_pair):
     qa, sa, qb, sb, offs = _contig_problem([100, 0, 300, 128, 1], N=272, K=384, seed=5, extra_rows=128)
     with pair(use_pair):
@@ -186,7 +188,8 @@ def _masked_problem(E, cap, N, K, seed):
     return qa.reshape(E, cap, K), sa.reshape(E, cap, -1), np.stack(qbs), np.stack(sbs)
 
 
-@pytest.mark.parametrize("bn,use_pair", [(None, 1), (256, 1), (256, 0), (192, 0), (128, 1), (64, 1), (None, 2), (256, 2)])
+@pytest.mark.parametrize("bn,use_pair", [(None, 1), (256, 1), (256, 0), (192, 0), (160, 0), (128, 1), (64, 1), (None, 2),
+                                          (256, 2)])
 def test_masked_small(bn, use_pair):
     E, cap, N, K = 5, 160, 272, 384
     masked = [0, 1, 160, 37, 129]
