@@ -19,7 +19,7 @@
  *                  fp8_quantize_1x128_e5m2, fp8_gemm_nt_dgrad, fp8_grouped_gemm_contiguous_dgrad,
  *                  fp8_grouped_gemm_wgrad
  *   status         fp8g_get_status, fp8g_status_string, fp8g_selftest_bounded_waits, fp8g_last_config,
- *                  fp8g_last_split
+ *                  fp8g_last_split, fp8g_last_swap_ab
  *
  * Sources (page title, section):
  *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
@@ -418,6 +418,18 @@ int fp8g_last_config(int* block_n, int* stages, int* grid);
  * FP8G_ERR_INVALID_ARG for a null pointer.
  */
 int fp8g_last_split(int* split);
+
+/*
+ * fp8g_last_swap_ab -- 1 when the last GEMM call on this thread ran swapped decode tiles: a
+ * block-scaled dense GEMM (fp8_gemm_nt, fp8_gemm_nt_noalloc, fp8_gemm_nt_dgrad) with M <= 64
+ * computed as D^T = B A^T, the weight rows taking the MMA's 128 rows and the tokens its 64
+ * columns ("DeepGEMM FP8 walk-through" sec. 4.2: small M kept efficient; sec. 3.2: work spread
+ * over the SMs from the shape), else 0.  Same results as the unswapped tiles up to FP32
+ * summation order.  Opt-in: FP8G_SWAP_AB=1 (and no tile width forced with FP8G_BLOCK_N); the
+ * default 64-wide tiles measured faster on the decode shape.  Diagnostic only; returns FP8G_OK, or
+ * FP8G_ERR_INVALID_ARG for a null pointer.
+ */
+int fp8g_last_swap_ab(int* swapped);
 
 #ifdef __cplusplus
 }

@@ -58,7 +58,13 @@ namespace {
 // kKGrouped: the weight gradient of a grouped layer -- one output matrix per expert, the
 // contraction running over that expert's token range (offsets in the group table), both
 // operands with one scale per row and 128-token block.
-enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3, kKGrouped = 4 };
+// kSwapAB (opt-in, FP8G_SWAP_AB=1): dense with M <= 64 computed as D^T = B A^T: the weight rows
+// take the MMA's M = 128 (a tile is a 128-row weight slab) and the tokens its N = 64, so each
+// tcgen05.mma covers twice the weight bytes of a 64-wide tile.  The tensor maps are swapped on
+// the host ("A" is the weight, "B" the activations); the promotion takes one weight-block scale
+// per tile and K block and one activation scale per column; the output is stored transposed.
+// The few tiles (N / 128) have their K blocks split over all SMs by the stream-K tail.
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kDenseSmallM = 3, kKGrouped = 4, kSwapAB = 5 };
 
 constexpr int BM = 128;  // rows per tile = TMEM lanes
 constexpr int BK = 128;  // K per stage = the scaling block
@@ -70,18 +76,20 @@ constexpr int kBandM = 16;  // m-blocks per raster band of CTA pairs (L2 reuse o
 // (its operands come mostly from L2) make room for a staging box per 32 columns in every store
 // warp, so a tile's boxes are stored without waiting on one another, and for each epilogue
 // warp's 512 bytes of per-column B scales.
-template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
+template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false, bool SWAP = false>
 struct Cfg {
   // columns per epilogue warp.  192-wide tiles and 256 x 128 pair tiles: 64, 160-wide tiles: 32,
   // so that each warp reads its whole partial with one load and frees the TMEM buffer before any
   // FMA (a 128-column warp holds 128 accumulators and can load only half its partial at a time, so
   // the FMAs of the first half sit between the buffer's completion and its release).
+  // Swapped tiles (64 token columns): 32, eight warps (per thread 32 accumulators, 32 loaded values
+  // and two prefetched sets of 32 column scales, with the registers of the rebalance below).
   static constexpr int kEpiCols =
-      BN == 160 ? 32 : (((PAIR && BN == 128) || BN == 192) ? 64 : (BN >= 128 ? 128 : BN));
+      (BN == 160 || SWAP) ? 32 : (((PAIR && BN == 128) || BN == 192) ? 64 : (BN >= 128 ? 128 : BN));
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
   // Narrow tiles (few, long K loops: small-M shapes) split the K blocks between two sets of
   // promotion warps (even / odd K blocks), whose FP32 partial sums are added at the tile end.
-  static constexpr int kKSplit = BN == 64 ? 2 : 1;
+  static constexpr int kKSplit = (BN == 64 && !SWAP) ? 2 : 1;
   static constexpr int kEpiGroups = kColGroups * kKSplit;  // warpgroups of epilogue warps
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kStoreWarps = 4 * kColGroups;     // warps that write D
@@ -97,22 +105,24 @@ struct Cfg {
   // 384 x 168 = 64512, rebalanced to 128 x 40 + 256 x 232 = 64512.  BN = 192: 512 x 128 = 65536,
   // rebalanced to 128 x 32 + 384 x 160 = 65536 (64 accumulators and 64 loaded values a thread).
   // BN = 160: 768 x 80 = 61440, rebalanced to 128 x 40 + 640 x 88 = 61440 (32 accumulators and 32
-  // loaded values).  Otherwise: producer and MMA warps, then the epilogue warpgroups (any four
-  // consecutive warps cover the four TMEM lane quarters).
-  static constexpr bool kRebalance = BN == 256 || BN == 192 || BN == 160;
+  // loaded values).  Swapped tiles: 384 x 168, rebalanced as at BN = 256.  Otherwise: producer and
+  // MMA warps, then the epilogue warpgroups (any four consecutive warps cover the four TMEM lane
+  // quarters).
+  static constexpr bool kRebalance = BN == 256 || BN == 192 || BN == 160 || SWAP;
   static constexpr int kEpiWarp0 = kRebalance ? 4 : 1 + kMmaWarps;
   static constexpr int kThreads = 32 * kEpiWarp0 + 32 * kEpiWarps;
   static constexpr uint32_t kRegsLow = BN == 192 ? 32 : 40;
-  static constexpr uint32_t kRegsHigh = BN == 256 ? 232 : (BN == 192 ? 160 : 88);
+  static constexpr uint32_t kRegsHigh = (BN == 256 || SWAP) ? 232 : (BN == 192 ? 160 : 88);
   // A rows loaded per stage: the MMA always reads 128 rows, and with SMALL the upper 64 are
   // whatever follows in shared memory (those rows of D are computed but never stored).
   static constexpr int kARows = SMALL ? 64 : BM;
   // K blocks per pipeline stage.  One TMA box then covers kKPS consecutive 128-byte pieces of
   // every row (a kKPS * 128-byte run in global memory): streaming weights from HBM in 128-byte
   // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
-  static constexpr int kKPS = SMALL ? 2 : 1;
+  static constexpr int kKPS = (SMALL || SWAP) ? 2 : 1;
+  // (swapped tiles: 32 KB of weights and 16 KB of activations per stage)
   static constexpr int kStages =
-      SMALL ? 6 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 5 : 6))));
+      SMALL ? 6 : (SWAP ? 4 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 5 : 6)))));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 3 at 160, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
@@ -123,7 +133,8 @@ struct Cfg {
   static constexpr uint32_t kStageABytes = kKPS * kABytes;
   static constexpr uint32_t kStageBBytes = kKPS * kBBytes;
   static constexpr uint32_t kOutBytes = 32 * 32 * 2;  // one 32 x 32 bf16 box
-  static constexpr int kOutBoxes = KG ? kEpiCols / 32 : 1;  // staging boxes per store warp
+  // staging boxes per store warp (swapped tiles store with plain transposed stores: none)
+  static constexpr int kOutBoxes = SWAP ? 0 : (KG ? kEpiCols / 32 : 1);
   static constexpr uint32_t kOutWarpBytes = kOutBoxes * kOutBytes;
   // K-grouped: the scales of each stage's K block, staged next to its operands by the producer --
   // the tile's 128 A-row scales (a 512-byte TMA box) and its BN per-column B scales (a TMA box).
@@ -152,12 +163,17 @@ struct Cfg {
   static_assert((BN != 192 && BN != 160) || (!SMALL && !PAIR && !KG),
                 "160- and 192-wide tiles: single-CTA block-scaled forms");
   static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
+  static_assert(!SWAP || (BN == 64 && !SMALL && !PAIR && !KG), "swapped tiles: 64 token columns, single CTA");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
   static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
 };
 
+// The configuration of a kernel instantiation.
+template <int BN, int MODE, bool PAIR>
+using CfgOf = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped, MODE == kSwapAB>;
+
 struct GemmArgs {
-  int32_t rows;      // rows of A / D (M, M_total or E*cap)
+  int32_t rows;      // rows of A / D (M, M_total or E*cap; swapped: the weight rows N)
   int32_t N, KB, NBs, E, cap;
   int32_t num_m;     // m-blocks (dense / contiguous)
   int32_t num_n;     // n-blocks of BN
@@ -455,11 +471,11 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* f, const GemmArgs& a, 
 }
 
 template <int BN, int MODE, bool PAIR = false, bool EPI = false>
-__global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>::kThreads, 1)
+__global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmSB, const GemmArgs a) {
-  using C = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>;
+  using C = CfgOf<BN, MODE, PAIR>;
   static_assert(!EPI || (C::kKSplit == 1 && C::kMmaWarps == 1 && !PAIR),
                 "epilogue scaling: one K part, one issuer, single-CTA tiles");
   static_assert(MODE != kKGrouped || (!EPI && !PAIR && C::kMmaWarps == 1),
@@ -491,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
   // epilogue-scaled variant); else one lane of the promotion warps once the stage's MMAs have
   // completed (block forms), or every promotion warp once it has also read the stage's scales
   // (K-grouped).
-  constexpr bool kCommitFrees = EPI || C::kMmaWarps > 1 || PAIR;
+  constexpr bool kCommitFrees = EPI || C::kMmaWarps > 1 || PAIR || C::kKPS > 1;
   constexpr uint32_t kEmptyArrivals = kCommitFrees ? 1u : (kStaged ? static_cast<uint32_t>(C::kEpiWarps) : 1u);
   // misc: [0] TMEM base, [1] abort flag, [2] group table out of contract
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -633,7 +649,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
     // run on lane 0 alone, test their next barriers ahead (wait_seen) and free stages by an MMA
     // commit; one issuer leaves the stage release to the promotion warps.
     constexpr bool kLone = MW > 1;
-    static_assert(KPS == 1 || kLone, "multi-K-block stages are freed by the issuers' commits");
+    static_assert(KPS == 1 || kCommitFrees, "multi-K-block stages are freed by the issuers' commits");
     // the tensor maps view A as [K/128][rows][128] and B as [E][K/128][N][128] (outer to
     // inner), so one box holds KPS K blocks of the tile's rows, K block by K block
     if (warp == 0 && leader) {
@@ -731,41 +747,49 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
           }
         }
       } else if constexpr (!kLone) {
-        uint32_t it = 0;
+        // stage `it` holds the K blocks kb .. kb + nk - 1 of the piece (nk = min(KPS, K blocks
+        // left in it)); `kit` counts K blocks, the TMEM buffer sequence as the epilogue counts it
+        uint32_t it = 0, kit = 0;
         bool ok = true;
         Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
         Piece pc;
         while (ok && next_piece(w, pc)) {
           Tile ti;
           if (!fetch_tile(pc, ti)) continue;
-          for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
+          for (int32_t kb = pc.kb0; kb < pc.kb1; kb += KPS, ++it) {
             const uint32_t s = it % S, ph = (it / S) & 1u;
-            const uint32_t b = it % NB, tph = (it / NB) & 1u;
             // the operand stage first: it is nearly always complete, and testing it costs a round
             // trip that would otherwise sit between the buffer's release and the MMAs
             if (!(wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
-            if (!(wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t ad = adesc0 + ((s * C::kStageABytes) >> 4);
-            const uint64_t bd = bdesc0 + ((s * C::kStageBBytes) >> 4);
-            const uint32_t d_tmem = tmem_base + b * BN;
-            if constexpr (PAIR) {
+            const int32_t nk = min(KPS, pc.kb1 - kb);
+            for (int32_t j = 0; j < nk; ++j, ++kit) {
+              const uint32_t b = kit % NB, tph = (kit / NB) & 1u;
+              if (!(wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t ad = adesc0 + ((s * C::kStageABytes + j * C::kABytes) >> 4);
+              const uint64_t bd = bdesc0 + ((s * C::kStageBBytes + j * C::kBBytes) >> 4);
+              const uint32_t d_tmem = tmem_base + b * BN;
+              if constexpr (PAIR) {
 #pragma unroll
-              for (int k = 0; k < BK / 32; ++k)
-                mma_f8f6f4_pair(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-              mma_commit_pair(leader, empty(s), 0x3);  // both CTAs' stage s is free
-              mma_commit_pair(leader, tfull(b), 0x3);  // both CTAs' partial is ready
-            } else {
+                for (int k = 0; k < BK / 32; ++k)
+                  mma_f8f6f4_pair(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                mma_commit_pair(leader, empty(s), 0x3);  // both CTAs' stage s is free
+                mma_commit_pair(leader, tfull(b), 0x3);  // both CTAs' partial is ready
+              } else {
 #pragma unroll
-              for (int k = 0; k < BK / 32; ++k)
-                mma_f8f6f4(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
-              // one commit per K block; the promotion warps free the stage once it has completed
-              mma_commit(leader, tfull(b));
+                for (int k = 0; k < BK / 32; ++k)
+                  mma_f8f6f4(leader, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                // one commit per K block; with one K block per stage the promotion warps free the
+                // stage once it has completed
+                mma_commit(leader, tfull(b));
+              }
             }
+            if (!ok) break;
+            if constexpr (KPS > 1) mma_commit(leader, empty(s));  // the stage's MMAs have read it
           }
         }
-        if (!ok && it > 0 && leader) {  // wait for the MMAs already issued before TMEM is released
-          const uint32_t last = it - 1;
+        if (!ok && kit > 0 && leader) {  // wait for the MMAs already issued before TMEM is released
+          const uint32_t last = kit - 1;
           const long long t0 = clock64();
           while (!mbar_try_wait(tfull(last % NB), (last / NB) & 1u) && clock64() - t0 < a.budget) {
           }
@@ -898,6 +922,63 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
         tc_fence_before();
         __syncwarp();
         release_tmem(b);
+      } else if constexpr (MODE == kSwapAB) {
+        // D^T tile: this thread's row is weight row `grow`, its columns the tokens ncol0 .. +31.
+        // Per K block acc += P * (sw * sa[m]): sw the scale of the tile's 128 x 128 weight block (one
+        // per tile), sa[m] the tokens' scales (one per column, the same for every thread: broadcast
+        // loads).  Both come from global memory two K-block steps ahead, in two register sets used
+        // alternately (the loop below is unrolled by two, as in the block forms).
+        constexpr int NC = C::kEpiCols;
+        static_assert(NC == 32 && C::kKSplit == 1, "swapped tiles: 32 columns a warp");
+#pragma unroll
+        for (int j = 0; j < NC / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+        const float* swp = a.sB + static_cast<int64_t>(ti.a_row / BM) * a.KB;
+        const float* scp = a.sA + ncol0;
+        const int32_t ncv = a.N - ncol0;  // token columns of this warp that exist
+        auto load_sc = [&](int32_t kbi, float (&c)[NC], float& w) {
+          const bool in = kbi < pc.kb1;
+          w = ld_nc_f32_or0(swp + kbi, in);
+          const float* p = scp + static_cast<int64_t>(kbi) * a.ld_sa;
+          if (in && ncv >= NC) {  // (16-byte aligned: ld_sa and ncol0 are multiples of 4)
+#pragma unroll
+            for (int j = 0; j < NC / 4; ++j) {
+              const float4 t = __ldg(reinterpret_cast<const float4*>(p) + j);
+              c[4 * j] = t.x;
+              c[4 * j + 1] = t.y;
+              c[4 * j + 2] = t.z;
+              c[4 * j + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) c[j] = ld_nc_f32_or0(p + j, in && j < ncv);
+          }
+        };
+        float c0[NC], c1[NC], w0, w1;
+        load_sc(pc.kb0, c0, w0);
+        load_sc(pc.kb0 + 1, c1, w1);
+        auto step = [&](int32_t kb, float (&c)[NC], float& w) -> bool {
+          const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
+          const uint32_t b = it % NB, tph = (it / NB) & 1u;
+          if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) return false;
+          tc_fence_after();
+          float v[NC];
+          tmem_ld32_sync(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0, v);
+          tc_fence_before();
+          __syncwarp();
+          release_tmem(b);
+          const float2 w2 = make_float2(w, w);
+#pragma unroll
+          for (int j = 0; j < NC / 2; ++j)
+            acc[j] = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]),
+                                __fmul2_rn(make_float2(c[2 * j], c[2 * j + 1]), w2), acc[j]);
+          load_sc(kb + 2, c, w);  // these registers' next use is two steps on
+          return true;
+        };
+        for (int32_t kb = pc.kb0; kb < pc.kb1; kb += 2) {
+          if (!step(kb, c0, w0)) { ok = false; break; }
+          if (kb + 1 >= pc.kb1) break;
+          if (!step(kb + 1, c1, w1)) { ok = false; break; }
+        }
       } else {
         // Per K block: acc += P * (sa * sb), with the partial P from TMEM.
         //   Block forms: sa (this thread's row) and sb (this warp's 128-column block) come from
@@ -1064,6 +1145,21 @@ __global__ void __launch_bounds__(Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kK
       // ---- epilogue: this warp holds rows q*32 .. q*32+31, columns ncol0 .. ncol0+kEpiCols-1
       const int nvalid = min(32, ti.rows - q * 32);
       if (nvalid <= 0 || !has_cols) continue;
+      if constexpr (MODE == kSwapAB) {
+        // transposed: D[m][n] for this thread's weight row n and the warp's tokens m; for a fixed
+        // token the 32 lanes write 32 consecutive bf16 of that row of D (64 bytes)
+        if (row_ok) {
+          __nv_bfloat16* dcol = a.D + grow;
+          const int32_t nv = min(C::kEpiCols, a.N - ncol0);
+#pragma unroll
+          for (int j = 0; j < C::kEpiCols; ++j) {
+            if (j < nv)
+              dcol[static_cast<int64_t>(ncol0 + j) * a.ldd] =
+                  __float2bfloat16_rn((j & 1) ? acc[j >> 1].y : acc[j >> 1].x);
+          }
+        }
+        continue;
+      }
       if constexpr (EPI) {
         // D = bf16(acc * fp32(sa[m] * sb[n])); sb is read with warp-uniform addresses (broadcast)
         const float sa_r = row_ok ? ld_nc_f32(a.sA + (a.sa_step ? grow : 0)) : 0.0f;
@@ -1166,9 +1262,9 @@ __global__ void bounded_wait_selftest_kernel(const GemmArgs a, uint32_t* out) {
 
 // ---------------------------------------------------------------- host side
 
-template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false>
+template <int BN, bool SMALL = false, bool PAIR = false, bool KG = false, bool SWAP = false>
 constexpr uint32_t smem_bytes(int table_entries) {
-  return Cfg<BN, SMALL, PAIR, KG>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
+  return Cfg<BN, SMALL, PAIR, KG, SWAP>::kOffTable + ((table_entries * 4 + 15) / 16) * 16;
 }
 
 constexpr int kMaxExperts = 2048;
@@ -1182,6 +1278,7 @@ constexpr int kMaxExperts160 = 512;
 static_assert(Cfg<160>::kOffTable + 4 * (kMaxExperts160 + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
+static_assert(Cfg<64, false, false, false, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, false, true>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
@@ -1191,7 +1288,7 @@ template <int BN, int MODE, bool PAIR = false, bool EPI = false>
 int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap& tB,
                   const CUtensorMap& tD, const CUtensorMap& tSA, const CUtensorMap& tSB, int grid,
                   int table_entries, cudaStream_t stream) {
-  using C = Cfg<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>;
+  using C = CfgOf<BN, MODE, PAIR>;
   auto kern = fp8_gemm_kernel<BN, MODE, PAIR, EPI>;
   static std::atomic<uint64_t> attr_set{0};  // one bit per device
   int dev = 0;
@@ -1217,7 +1314,7 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     }
     attr_set.fetch_or(bit);
   }
-  const uint32_t smem = smem_bytes<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped>(table_entries);
+  const uint32_t smem = smem_bytes<BN, MODE == kDenseSmallM, PAIR, MODE == kKGrouped, MODE == kSwapAB>(table_entries);
   if constexpr (PAIR) {  // clusters of two CTAs (the grid is even)
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1330,13 +1427,24 @@ int32_t band_rows(int32_t num_m, int64_t K, int mode) {
   return a_bytes <= (int64_t{48} << 20) ? (num_m > 0 ? num_m : 1) : kBandM;
 }
 
+// FP8G_SWAP_AB=1 runs M <= 64 with swapped tiles (read on every call); otherwise the 64-wide small-M
+// tiles.  Off by default: on 64 x 7168 x 7168 the swapped kernel took 21 us with its K blocks split
+// over all SMs (28 us unsplit, on 56 SMs) against 19.7 us for the 64-wide tiles on 112 SMs (device
+// times); the split's flag memset and cooperative launch add ~4 us more per call.  Both tile forms
+// stream ~27 bytes per cycle per SM through TMA, so the larger weight share of a swapped stage
+// (two thirds against one half) did not pay for the split.
+bool env_swap_ab() {
+  const char* e = std::getenv("FP8G_SWAP_AB");
+  return e && e[0] == '1' && e[1] == 0;
+}
+
 // FP8G_STREAMK=0 turns the stream-K tail off (read on every call).
 bool env_streamk() {
   const char* e = std::getenv("FP8G_STREAMK");
   return !(e && e[0] == '0' && e[1] == 0);
 }
 
-thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0, t_last_split = 0;
+thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0, t_last_split = 0, t_last_swap = 0;
 
 // FP8G_PAIR=1 runs 256-wide tiles as 256 x 256 CTA-pair tiles, FP8G_PAIR=2 as 256 x 128 pair
 // tiles (four TMEM partial buffers per CTA).  Off by default: measured no faster than single-CTA
@@ -1408,8 +1516,12 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   int bn = choose_block_n(m_blocks, o.N, dev->sm_count, (EPI || MODE == kKGrouped) ? 128 : 64);
   if ((EPI || MODE == kKGrouped) && (bn == 192 || bn == 160)) bn = 256;  // those forms: 128 and 256 wide
   if (bn == 160 && MODE != kDense && o.E > kMaxExperts160) bn = 256;    // group table too large
-  // decode shapes: at most 64 rows of A, narrow tiles -> the small-M variant (64-row A boxes)
-  const bool small_m = MODE == kDense && bn == 64 && o.rows <= 64;
+  // decode shapes (at most 64 rows of A, block-scaled dense): with FP8G_SWAP_AB=1 (and no tile width
+  // forced by FP8G_BLOCK_N) swapped tiles, weight rows on the MMA's M; else 64-wide tiles in the
+  // small-M variant (64-row A boxes)
+  const bool swap = MODE == kDense && !EPI && o.rows <= 64 && env_block_n() == 0 && env_swap_ab();
+  if (swap) bn = 64;
+  const bool small_m = MODE == kDense && !swap && bn == 64 && o.rows <= 64;
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
   // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2); the epilogue-scaled variant has single-CTA tiles
   const int pmode = (EPI || MODE == kKGrouped) ? 0 : env_pair();
@@ -1442,11 +1554,31 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   a.test_skip_stage = env_test_skip_stage();
   a.band_m = band_rows(a.num_m, o.K, MODE == kDenseSmallM ? kDense : MODE);
   if (MODE == kKGrouped) a.num_tiles = static_cast<int32_t>(o.E) * a.num_m * a.num_n;
+  if (swap) {
+    // D^T = B A^T: rows are the weight rows, columns the tokens; one 128-row weight slab a tile.
+    // sA (token scales [K/128][ld_sa]) and sB (weight block scales [N/128][K/128]) keep their
+    // meaning; the A and B operand formats trade places in the instruction descriptor.
+    a.rows = static_cast<int32_t>(o.N);
+    a.N = static_cast<int32_t>(o.rows);
+    a.num_m = static_cast<int32_t>((o.N + BM - 1) / BM);
+    a.num_n = 1;
+    a.num_tiles = a.num_m;
+    a.band_m = band_rows(a.num_m, o.K, kDense);
+    a.idesc_fmt = (((o.idesc_fmt >> 7) & 7u) << 10) | (((o.idesc_fmt >> 10) & 7u) << 7);
+  }
 
   // K blocks per stage of the variant launched below (its Cfg::kKPS)
-  const uint32_t kps = small_m ? Cfg<64, true>::kKPS : 1u;
+  const uint32_t kps = small_m ? Cfg<64, true>::kKPS : (swap ? Cfg<64, false, false, false, true>::kKPS : 1u);
   CUtensorMap tA, tB, tD;
-  {
+  if (swap) {
+    // the MMA's A: the weights as [K/128][N][128], a box of kps K blocks of a 128-row slab
+    const uint64_t dims[3] = {BK, static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.K / BK)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(o.ldb), BK};
+    const uint32_t box[3] = {BK, static_cast<uint32_t>(BM), kps};
+    if ((st = encode_tmap(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, o.B, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
+      return st;
+  } else {
     // A as [K/128][rows][128]: a box is kps K blocks of the tile's rows
     const uint64_t dims[3] = {BK, static_cast<uint64_t>(o.rows), static_cast<uint64_t>(o.K / BK)};
     const uint64_t strides[2] = {static_cast<uint64_t>(o.lda), BK};
@@ -1455,7 +1587,16 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
                           CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
       return st;
   }
-  {
+  if (swap) {
+    // the MMA's B: the activations as [1][K/128][M][128], a box of kps K blocks of 64 token rows
+    // (rows past M read as zero)
+    const uint64_t dims[4] = {BK, static_cast<uint64_t>(o.rows), static_cast<uint64_t>(o.K / BK), 1};
+    const uint64_t strides[3] = {static_cast<uint64_t>(o.lda), BK, static_cast<uint64_t>(o.lda * o.rows)};
+    const uint32_t box[4] = {BK, 64u, kps, 1};
+    if ((st = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, o.A, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != FP8G_OK)
+      return st;
+  } else {
     // B as [E][K/128][N][128]
     const uint64_t dims[4] = {BK, static_cast<uint64_t>(o.N), static_cast<uint64_t>(o.K / BK),
                               static_cast<uint64_t>(MODE == kKGrouped ? 1 : o.E)};
@@ -1515,8 +1656,9 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
     if (u < umin) u = umin;
     return U > 0 && KB - u >= a.sk_min_gain;
   };
-  // (160-wide tiles have two MMA issuers, which take whole tiles)
-  if (MODE != kKGrouped && !pair && !small_m && bn >= 128 && bn != 160 && env_streamk() &&
+  // (160-wide tiles have two MMA issuers, which take whole tiles; swapped tiles split too: their
+  // N / 128 weight slabs are fewer than the SMs)
+  if (MODE != kKGrouped && !pair && !small_m && (swap || (bn >= 128 && bn != 160)) && env_streamk() &&
       (MODE == kMasked || tail_splits(a.num_tiles))) {
     int dev_id = 0;
     cudaGetDevice(&dev_id);
@@ -1551,6 +1693,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   t_last_bn = bn;
   t_last_grid = grid;
   t_last_split = a.sk;
+  t_last_swap = swap ? 1 : 0;
   if constexpr (MODE == kKGrouped) {
     if (bn == 256) {
       t_last_stages = Cfg<256, false, false, true>::kStages;
@@ -1566,6 +1709,12 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
     t_last_stages = Cfg<128>::kStages;
     return launch_kernel<128, MODE, false, true>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
   } else {
+    if constexpr (MODE == kDense) {
+      if (swap) {
+        t_last_stages = Cfg<64, false, false, false, true>::kStages;
+        return launch_kernel<64, kSwapAB>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
+      }
+    }
     switch (bn) {
       case 256:
         if (pair) {
@@ -1822,6 +1971,12 @@ extern "C" int fp8g_selftest_bounded_waits(int64_t budget_cycles, uint32_t* out,
 extern "C" int fp8g_last_split(int* split) {
   if (!split) return FP8G_ERR_INVALID_ARG;
   *split = t_last_split;
+  return FP8G_OK;
+}
+
+extern "C" int fp8g_last_swap_ab(int* swapped) {
+  if (!swapped) return FP8G_ERR_INVALID_ARG;
+  *swapped = t_last_swap;
   return FP8G_OK;
 }
 

@@ -102,6 +102,7 @@ def test_last_config_null_pointer(lib):
     null = ctypes.POINTER(ctypes.c_int)()
     assert lib.fp8g_last_config(null, null, null) == INVALID
     assert lib.fp8g_last_split(null) == INVALID
+    assert lib.fp8g_last_swap_ab(null) == INVALID
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):

@@ -67,7 +67,8 @@ def _dgrad_problem(M, N, K, seed):
 @pytest.mark.parametrize("M,N,K,bn", [
     (128, 256, 512, None), (200, 208, 384, 256), (200, 208, 384, 128), (129, 272, 256, 64),
     (64, 1792, 2048, None),  # the small-M variant (two lone issuers)
-    (17, 128, 1152, 64), (513, 384, 256, None),
+    (17, 128, 1152, 64),
+    (513, 384, 256, None),
 ])
 def test_dgrad_gemm(M, N, K, bn):
     qa, sa, qb, sb = _dgrad_problem(M, N, K, M + 3 * N + K)
@@ -77,6 +78,20 @@ def test_dgrad_gemm(M, N, K, bn):
     torch.cuda.synchronize()
     check_status()
     assert_gemm_close(bf16_to_np(D), gemm_nt_dgrad(qa, sa, qb, sb), f"dgrad {M}x{N}x{K} bn={bn}")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1792, 2048), (40, 1792, 7168)])
+def test_dgrad_swapped_decode_tiles(M, N, K):
+    # FP8G_SWAP_AB=1: the e5m2 gradient is the MMA's B operand (its format field moves with it);
+    # (40, 1792, 7168) splits its K blocks over the SMs
+    qa, sa, qb, sb = _dgrad_problem(M, N, K, 2 * M + N + K)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with env_var("FP8G_SWAP_AB", "1"):
+        g.fp8_gemm_nt_dgrad(u8(qa), sa_to_device(sa), u8(qb), torch.from_numpy(sb).cuda(), D)
+        torch.cuda.synchronize()
+        assert g.fp8g_last_config()["swap_ab"]
+    check_status()
+    assert_gemm_close(bf16_to_np(D), gemm_nt_dgrad(qa, sa, qb, sb), f"dgrad swapped {M}x{N}x{K}")
 
 
 def test_dgrad_stream_k_tail():

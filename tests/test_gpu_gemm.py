@@ -109,6 +109,49 @@ def test_dense_all_scales_equal_power_of_two_case():
     assert torch.equal(D1, D2)
 
 
+# ---------------------------------------------------------------- swapped decode tiles
+# FP8G_SWAP_AB=1, M <= 64: D^T = B A^T, the weight rows on the MMA's M = 128 and the
+# tokens on its N = 64 (rows past M read as zero and are never stored), stored transposed.  The
+# N / 128 weight slabs are fewer than the SMs, so their K blocks are split over all SMs (stream-K)
+# when that saves enough; (24, 6016, 5120) splits into pieces of 13 K blocks, so pieces start on
+# odd K blocks inside the two-K-block stages.
+
+@pytest.mark.parametrize("M,N,K,split", [
+    (1, 16, 128, False), (16, 208, 384, False), (17, 384, 1152, False), (33, 528, 2560, False),
+    (40, 1792, 7168, True), (64, 2048, 7168, True), (24, 6016, 5120, True),
+])
+def test_dense_swapped_decode_tiles(M, N, K, split):
+    qa, sa, qb, sb = _problem(M, N, K, seed=5 * M + N + K)
+    with env_var("FP8G_SWAP_AB", "1"):
+        D = _dense_gpu(qa, sa, qb, sb)
+        cfg = g.fp8g_last_config()
+    assert cfg["swap_ab"] and cfg["split"] == split, cfg
+    assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"swapped {M}x{N}x{K}")
+
+
+def test_dense_swapped_tiles_switch_and_strides():
+    # by default M <= 64 takes the 64-wide small-M tiles; strided operands and ld_sa > M in the
+    # swapped form (FP8G_SWAP_AB=1)
+    M, N, K = 20, 400, 1024
+    qa, sa, qb, sb = _problem(M, N, K, seed=31)
+    D0 = _dense_gpu(qa, sa, qb, sb)
+    assert not g.fp8g_last_config()["swap_ab"]
+    A = torch.zeros((M, K + 32), dtype=torch.uint8, device="cuda")
+    A[:, :K] = u8(qa)
+    B = torch.zeros((N, K + 64), dtype=torch.uint8, device="cuda")
+    B[:, :K] = u8(qb)
+    D = torch.full((M, N + 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    with env_var("FP8G_SWAP_AB", "1"):
+        g.fp8_gemm_nt(A[:, :K], sa_to_device(sa, ld_sa=36), B[:, :K], torch.from_numpy(sb).cuda(), D[:, :N])
+        torch.cuda.synchronize()
+        assert g.fp8g_last_config()["swap_ab"]
+    check_status()
+    ref = gemm_nt(qa, sa, qb, sb)
+    assert_gemm_close(bf16_to_np(D[:, :N]), ref, "swapped, strided")
+    assert_gemm_close(bf16_to_np(D0), ref, "small-M tiles")
+    assert torch.all(D[:, N:] == 7.0)
+
+
 # ---------------------------------------------------------------- contiguous
 
 def _contig_problem(sizes, N, K, seed, extra_rows=0):
