@@ -502,13 +502,14 @@ def measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak, reps=20):
     sA = torch.empty((K // 128, m_cap), dtype=torch.float32, device=dev)
     offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
     rows = torch.empty(m_cap, dtype=torch.int32, device=dev)
+    entry = torch.empty(ids.numel(), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     lib = g.lib()
 
     def call():
         st = lib.fp8_route_gather_quantize_1x128(x.data_ptr(), T, K, K, ids.data_ptr(), w.topk, w.E, q.data_ptr(),
-                                                 K, sA.data_ptr(), m_cap, offs.data_ptr(), rows.data_ptr(), m_cap,
-                                                 stream.cuda_stream)
+                                                 K, sA.data_ptr(), m_cap, offs.data_ptr(), rows.data_ptr(),
+                                                 entry.data_ptr(), m_cap, stream.cuda_stream)
         if st != 0:
             raise RuntimeError(f"route_gather_quantize failed: {g.STATUS.get(st, st)}")
 
@@ -524,8 +525,9 @@ def measure_next_rows(names, g, dev, flush, hbm_peak, fp8_peak, reps=20):
     if g.fp8g_get_status() != 0:
         raise RuntimeError("device status not OK after route_gather_quantize")
     us = statistics.median(e[0].elapsed_time(e[1]) for e in evs) * 1e3
-    # algorithmic bytes: each token row read once, the ids, the codes / scales / token map written
-    nbytes = T * K * 2 + ids.numel() * 4 + m_cap * K + m_cap * (K // 128) * 4 + m_cap * 4 + (w.E + 1) * 4
+    # algorithmic bytes: each token row read once, the ids, the codes / scales / both maps written
+    nbytes = (T * K * 2 + ids.numel() * 4 + m_cap * K + m_cap * (K // 128) * 4 + m_cap * 4 + (w.E + 1) * 4
+              + ids.numel() * 4)
     gbs = nbytes / (us * 1e-6) / 1e9
     out["route_gather_quantize_1x128"] = {
         "workload": f"moe_contiguous routing: {T} tokens x top-{w.topk} of {w.E} experts, K={K}, M_cap={m_cap}",

@@ -131,9 +131,15 @@ int fp8_quantize_1x128_masked(const void* x, int32_t E, int64_t cap, int64_t K, 
  *                  group_offsets[e] .. group_offsets[e+1]-1 (multiples of 128)
  *   row_token      int32 [M_cap], DEVICE memory, output: the token of each row, -1 for a
  *                  padding row
+ *   entry_row      int32 [T*topk], DEVICE memory, output: the row of each entry (token t,
+ *                  slot j at t*topk + j), -1 for a dropped entry -- the inverse of row_token,
+ *                  the map a combine step needs to bring the experts' output rows back to
+ *                  their tokens (may be null when T == 0)
  *   M_cap          rows of q / sA / row_token: a multiple of 128 and at least
  *                  T*topk + 127*E (every group padded to 128 fits)
  *
+ * Each token row is read and quantised once and its codes and scales are stored to every
+ * row of the token (its 1x128 scales depend only on the row's own values).
  * Inside a group the rows hold the expert's tokens in ascending order (a token that names
  * one expert twice gets two rows), then zero rows up to the next multiple of 128.  Every
  * row with token -1 -- padding, and the rows from group_offsets[E] to M_cap -- has scale
@@ -141,12 +147,13 @@ int fp8_quantize_1x128_masked(const void* x, int32_t E, int64_t cap, int64_t K, 
  * are skipped and their output rows left untouched.  Expert ids outside [0, E) are
  * dropped and set FP8G_ERR_DEVICE_ASSERT.  T >= 0, topk >= 1, 1 <= E <= 2048,
  * K % 128 == 0, M_cap * (K/128) < 2^31.  x, q, sA 16-byte aligned (x may be null when
- * T == 0).
+ * T == 0); the int32 arrays 4-byte aligned.
  */
 int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t K, int64_t ldx,
                                     const int32_t* topk_ids, int32_t topk, int32_t E, void* q,
                                     int64_t ldq, float* sA, int64_t ld_sa, int32_t* group_offsets,
-                                    int32_t* row_token, int64_t M_cap, void* stream);
+                                    int32_t* row_token, int32_t* entry_row, int64_t M_cap,
+                                    void* stream);
 
 /*
  * fp8_quantize_128x128 -- weight quantisation, one scale per 128x128 block

@@ -60,7 +60,7 @@ _SIGNATURES = {
     "fp8_gemm_nt": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_gemm_nt_noalloc": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_route_gather_quantize_1x128": [_P, _I64, _I64, _I64, _P, _I32, _I32, _P, _I64, _FP, _I64, _P, _P,
-                                        _I64, _P],
+                                        _P, _I64, _P],
     "fp8_grouped_gemm_contiguous": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_masked": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
     "fp8_quantize_per_row": [_P, _I64, _I64, _I64, _P, _I64, _FP, _P],
@@ -436,8 +436,9 @@ def route_capacity(T: int, topk: int, E: int) -> int:
 
 def route_gather_quantize_1x128(x: torch.Tensor, topk_ids: torch.Tensor, E: int, m_cap: int | None = None):
     """bf16 tokens [T,K] + int32 expert choices [T,topk] (device) -> (q uint8 [m_cap,K],
-    sA f32 [K/128, m_cap], group_offsets int32 [E+1], row_token int32 [m_cap]), all on the device:
-    the contiguous grouped layout, quantised.  m_cap defaults to route_capacity(T, topk, E)."""
+    sA f32 [K/128, m_cap], group_offsets int32 [E+1], row_token int32 [m_cap],
+    entry_row int32 [T,topk]), all on the device: the contiguous grouped layout, quantised, and the
+    row of each (token, slot) entry (-1: dropped).  m_cap defaults to route_capacity(T, topk, E)."""
     T, K = x.shape
     _need(topk_ids.dtype == torch.int32 and topk_ids.dim() == 2 and topk_ids.shape[0] == T
           and topk_ids.is_contiguous(), "topk_ids: int32 [T,topk] contiguous")
@@ -447,10 +448,11 @@ def route_gather_quantize_1x128(x: torch.Tensor, topk_ids: torch.Tensor, E: int,
     sA = torch.empty((K // 128, m), dtype=torch.float32, device=x.device)
     offs = torch.empty(E + 1, dtype=torch.int32, device=x.device)
     rows = torch.empty(m, dtype=torch.int32, device=x.device)
+    entry = torch.empty((T, topk), dtype=torch.int32, device=x.device)
     _check(lib().fp8_route_gather_quantize_1x128(_ptr(x), T, K, x.stride(0), _ptr(topk_ids), topk, E, _ptr(q),
-                                                 q.stride(0), _ptr(sA), m, _ptr(offs), _ptr(rows), m,
-                                                 _stream(x)), "fp8_route_gather_quantize_1x128")
-    return q, sA, offs, rows
+                                                 q.stride(0), _ptr(sA), m, _ptr(offs), _ptr(rows), _ptr(entry),
+                                                 m, _stream(x)), "fp8_route_gather_quantize_1x128")
+    return q, sA, offs, rows, entry
 
 
 def quantize_128x128(w: torch.Tensor):

@@ -206,16 +206,21 @@ __device__ __forceinline__ void advance(RowKb& p, uint32_t dm, uint32_t dkb, uin
   }
 }
 
-// GATHER: output row m holds input row row_src[m] (a zero row where row_src[m] < 0).
+// SCATTER (route-gather-quantize): the M input rows are tokens; token m's codes and scales go to
+// the output rows row_src[m * topk + j], j < topk (none where -1), so a token chosen by several
+// experts is read and quantised once.  Afterwards every output row r < rows_out with
+// zero_src[r] < 0 (group padding, rows past the last group) is written as a zero row: codes 0,
+// scale 0.
 // FMT: e4m3 (s = amax / 448) or e5m2 (gradients, s = amax / 57344).
 // MASKED: rows are experts x cap and only rows r < row_src[e] of expert e (its count, clamped to
 // [0, cap]) are quantised; the others are left as they are.  Grid row blockIdx.y is expert e,
 // striding over that expert's valid (row, K block) items only.
-template <bool GATHER, int FMT = kE4M3, bool MASKED = false>
+template <bool SCATTER, int FMT = kE4M3, bool MASKED = false>
 __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx,
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa,
-    const int32_t* __restrict__ row_src, uint32_t cap = 0) {
+    const int32_t* __restrict__ row_src, uint32_t cap = 0, uint32_t topk = 1,
+    const int32_t* __restrict__ zero_src = nullptr, uint32_t rows_out = 0) {
   const int sub = threadIdx.x & (kQLanes - 1);
   const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) / kQLanes;
   const uint32_t n_groups = gridDim.x * kQGroupsPerBlock;
@@ -244,9 +249,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
       }
       live[u] = base + u * n_groups < total;
       raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
-      int64_t src_row = it[u].m + row0;
-      if (GATHER && live[u]) src_row = __ldg(row_src + it[u].m);
-      if (live[u] && src_row >= 0) {
+      const int64_t src_row = it[u].m + row0;
+      if (live[u]) {
         const __nv_bfloat16* src = x + src_row * ldx + it[u].kb * 128 + sub * 8;
         raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
         raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 64));
@@ -271,11 +275,33 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
         uint32_t c[4];
         quant_n<16, FMT>(f, s, FMT == kE4M3 ? direct_mode(a, s) : 0u, c);
         const uint32_t m = it[u].m + row0;
-        uint8_t* dst = q + static_cast<int64_t>(m) * ldq + it[u].kb * 128 + sub * 8;
-        *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
-        *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
-        if (sub == 0) sA[static_cast<int64_t>(it[u].kb) * ld_sa + m] = s;
+        if constexpr (SCATTER) {
+          for (uint32_t j = 0; j < topk; ++j) {
+            const int32_t r = __ldg(row_src + static_cast<int64_t>(m) * topk + j);
+            if (r < 0) continue;
+            uint8_t* dst = q + static_cast<int64_t>(r) * ldq + it[u].kb * 128 + sub * 8;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+            *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
+            if (sub == 0) sA[static_cast<int64_t>(it[u].kb) * ld_sa + r] = s;
+          }
+        } else {
+          uint8_t* dst = q + static_cast<int64_t>(m) * ldq + it[u].kb * 128 + sub * 8;
+          *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+          *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
+          if (sub == 0) sA[static_cast<int64_t>(it[u].kb) * ld_sa + m] = s;
+        }
       }
+    }
+  }
+  if constexpr (SCATTER) {
+    // zero rows, a warp per row (the rows written above are all mapped, so none is written twice)
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t gwarp = (blockIdx.x * kQThreads + threadIdx.x) >> 5, nwarps = gridDim.x * (kQThreads / 32);
+    for (uint32_t r = gwarp; r < rows_out; r += nwarps) {
+      if (__ldg(zero_src + r) >= 0) continue;
+      uint4* qr = reinterpret_cast<uint4*>(q + static_cast<int64_t>(r) * ldq);
+      for (uint32_t v = lane; v < KB * 8u; v += 32u) qr[v] = make_uint4(0u, 0u, 0u, 0u);
+      for (uint32_t kb = lane; kb < KB; kb += 32u) sA[static_cast<int64_t>(kb) * ld_sa + r] = 0.0f;
     }
   }
 }
@@ -327,11 +353,12 @@ __global__ void __launch_bounds__(256) quantize_128x128_kernel(
 
 // ---------------------------------------------------------------- routing layout
 // One CTA builds the contiguous grouped layout from the expert choices ids[T*k] (token-major):
-// group_offsets[E+1] (each group's row count rounded up to 128) and row_token[M_cap] (the token
-// of each row; -1 for padding rows and for rows past the last group).  Inside a group the rows
-// follow the entries' order, i.e. ascending tokens.  Ids outside [0, E) are dropped and flag
-// FP8G_ERR_DEVICE_ASSERT; if the padded rows would not fit into M_cap, the layout is left empty
-// (all offsets 0) and the same status is raised.
+// group_offsets[E+1] (each group's row count rounded up to 128), row_token[M_cap] (the token of
+// each row; -1 for padding rows and for rows past the last group) and entry_row[T*k] (the row of
+// each entry, its inverse; -1 for a dropped entry).  Inside a group the rows follow the entries'
+// order, i.e. ascending tokens.  Ids outside [0, E) are dropped and flag FP8G_ERR_DEVICE_ASSERT;
+// if the padded rows would not fit into M_cap, the layout is left empty (all offsets 0, every
+// entry dropped) and the same status is raised.
 // ---- per-token / per-channel (one scale per row over the whole K) and per-tensor scales
 // ("DeepGEMM FP8 walk-through" sec. 2.2); same scale and code rules as the block forms.
 
@@ -448,7 +475,7 @@ constexpr int kRouteChunk = 4096;  // entries staged in shared memory per pass o
 
 __global__ void __launch_bounds__(kRouteThreads) route_layout_kernel(
     const int32_t* __restrict__ ids, int32_t n, int32_t topk, int32_t E, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ row_token, int64_t M_cap, unsigned int* status) {
+    int32_t* __restrict__ row_token, int32_t* __restrict__ entry_row, int64_t M_cap, unsigned int* status) {
   __shared__ int32_t s_count[kRouteMaxExperts];     // per-expert counts, then running ranks
   __shared__ int32_t s_off[kRouteMaxExperts + 1];   // padded prefix
   __shared__ int32_t s_chunk[kRouteChunk];
@@ -502,6 +529,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_kernel(
   const bool fits = static_cast<int64_t>(s_off[E]) <= M_cap;
   for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = fits ? s_off[e] : 0;
   for (int64_t r = tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
+  if (!fits)
+    for (int32_t i = tid; i < n; i += kRouteThreads) entry_row[i] = -1;
   for (int e = tid; e < E; e += kRouteThreads) s_count[e] = 0;  // now: rows handed out per expert
   __syncthreads();
   // rows in entry order: one warp walks the entries 32 at a time; lanes choosing the same expert
@@ -517,7 +546,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_kernel(
         if (e < 0 || e >= E) e = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0) row_token[s_off[e] + s_count[e] + rank] = (c0 + i) / topk;
+        if (e >= 0) {
+          const int32_t r = s_off[e] + s_count[e] + rank;
+          row_token[r] = (c0 + i) / topk;
+          entry_row[c0 + i] = r;
+        } else if (i < cn) {
+          entry_row[c0 + i] = -1;
+        }
         __syncwarp();
         if (e >= 0 && (peers >> lane) == 1u) s_count[e] += __popc(peers);
         __syncwarp();
@@ -535,7 +570,7 @@ constexpr int kRouteSmallExperts = 256;
 
 __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
     const int32_t* __restrict__ ids, int32_t n, int32_t topk, int32_t E, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ row_token, int64_t M_cap, unsigned int* status) {
+    int32_t* __restrict__ row_token, int32_t* __restrict__ entry_row, int64_t M_cap, unsigned int* status) {
   constexpr int W = kRouteThreads / 32;
   __shared__ int32_t s_wcnt[W][kRouteSmallExperts];  // counts, then each warp's first rank
   __shared__ int32_t s_off[kRouteSmallExperts + 1];
@@ -546,7 +581,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
   __syncthreads();
   const int32_t L = (n + W - 1) / W;
   const int32_t lo = warp * L, hi = min(n, lo + L);
-  for (int32_t i = lo + lane; i < hi; i += 32) {
+  // the first kIdCache * 32 entries of the warp's range are loaded once, all at the same time, and
+  // kept in registers for the row assignment below (a warp's range of 8192 top-2 entries is 256)
+  constexpr int kIdCache = 16;
+  int32_t idc[kIdCache];
+#pragma unroll
+  for (int j = 0; j < kIdCache; ++j) {
+    const int32_t i = lo + lane + 32 * j;
+    idc[j] = i < hi ? __ldg(ids + i) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < kIdCache; ++j) {
+    if (lo + lane + 32 * j < hi) {
+      if (idc[j] >= 0 && idc[j] < E) atomicAdd(&s_wcnt[warp][idc[j]], 1);
+      else s_bad = 1;
+    }
+  }
+  for (int32_t i = lo + lane + 32 * kIdCache; i < hi; i += 32) {
     const int32_t e = __ldg(ids + i);
     if (e >= 0 && e < E) atomicAdd(&s_wcnt[warp][e], 1);
     else s_bad = 1;
@@ -592,19 +643,34 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
   const bool fits = static_cast<int64_t>(s_off[E]) <= M_cap;
   for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = fits ? s_off[e] : 0;
   for (int64_t r = tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
+  if (!fits)
+    for (int32_t i = tid; i < n; i += kRouteThreads) entry_row[i] = -1;
   __syncthreads();
   if (fits) {
-    for (int32_t b = lo; b < hi; b += 32) {
+    // 32 entries at a time (warp-uniform): lanes choosing the same expert take consecutive rows in
+    // lane order (match_any); the last of them advances the warp's count for that expert
+    auto assign = [&](int32_t b, int32_t e) {
       const int32_t i = b + lane;
-      int32_t e = i < hi ? __ldg(ids + i) : -1;
-      if (e < 0 || e >= E) e = -1;
+      if (i >= hi || e < 0 || e >= E) e = -1;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
-      if (e >= 0) row_token[s_off[e] + s_wcnt[warp][e] + rank] = i / topk;
+      if (e >= 0) {
+        const int32_t r = s_off[e] + s_wcnt[warp][e] + rank;
+        row_token[r] = i / topk;
+        entry_row[i] = r;
+      } else if (i < hi) {
+        entry_row[i] = -1;
+      }
       __syncwarp();
       if (e >= 0 && (peers >> lane) == 1u) s_wcnt[warp][e] += __popc(peers);
       __syncwarp();
+    };
+#pragma unroll
+    for (int j = 0; j < kIdCache; ++j) {
+      if (lo + 32 * j >= hi) break;
+      assign(lo + 32 * j, idc[j]);
     }
+    for (int32_t b = lo + 32 * kIdCache; b < hi; b += 32) assign(b, b + lane < hi ? __ldg(ids + b + lane) : -1);
   }
   if (tid == 0 && (s_bad || !fits)) record_status(status, FP8G_ERR_DEVICE_ASSERT);
 }
@@ -713,7 +779,7 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
                                                const int32_t* topk_ids, int32_t topk, int32_t E,
                                                void* q, int64_t ldq, float* sA, int64_t ld_sa,
                                                int32_t* group_offsets, int32_t* row_token,
-                                               int64_t M_cap, void* stream) {
+                                               int32_t* entry_row, int64_t M_cap, void* stream) {
   if (T < 0 || T > 0x7FFFFFFF || K <= 0 || K % 128 != 0 || topk < 1 || E < 1 ||
       E > kRouteMaxExperts || ldx < K || ldq < K)
     return FP8G_ERR_INVALID_ARG;
@@ -721,11 +787,12 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
   if (n > 0x7FFFFFFF || M_cap % 128 != 0 || M_cap < n + int64_t{127} * E || ld_sa < M_cap ||
       M_cap * (K / 128) >= (int64_t{1} << 31))
     return FP8G_ERR_INVALID_ARG;
-  if (!q || !sA || !group_offsets || !row_token || (n > 0 && (!x || !topk_ids)))
+  if (!q || !sA || !group_offsets || !row_token || (n > 0 && (!x || !topk_ids || !entry_row)))
     return FP8G_ERR_INVALID_ARG;
   if ((x && !aligned16(x)) || !aligned16(q) || !aligned16(sA) || ldx % 8 != 0 || ldq % 16 != 0 ||
       ld_sa % 4 != 0 || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
-      (reinterpret_cast<uintptr_t>(group_offsets) & 3u) || (reinterpret_cast<uintptr_t>(row_token) & 3u))
+      (reinterpret_cast<uintptr_t>(group_offsets) & 3u) || (reinterpret_cast<uintptr_t>(row_token) & 3u) ||
+      (reinterpret_cast<uintptr_t>(entry_row) & 3u))
     return FP8G_ERR_ALIGNMENT;
   DeviceInfo* dev = nullptr;
   int st = current_device(&dev);
@@ -733,19 +800,22 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (E <= kRouteSmallExperts)
     route_layout_small_kernel<<<1, kRouteThreads, 0, s>>>(topk_ids, static_cast<int32_t>(n), topk, E,
-                                                          group_offsets, row_token, M_cap, dev->status);
+                                                          group_offsets, row_token, entry_row, M_cap,
+                                                          dev->status);
   else
     route_layout_kernel<<<1, kRouteThreads, 0, s>>>(topk_ids, static_cast<int32_t>(n), topk, E, group_offsets,
-                                                    row_token, M_cap, dev->status);
+                                                    row_token, entry_row, M_cap, dev->status);
   if (cudaGetLastError() != cudaSuccess) return FP8G_ERR_CUDA;
-  const int64_t items = M_cap * (K / 128);
+  // each token read and quantised once, stored to its rows; then the zero rows (a warp per row)
+  const int64_t items = T * (K / 128);
   const int64_t per_block = kQGroupsPerBlock * kQUnroll;
-  int64_t blocks = (items + per_block - 1) / per_block;
+  int64_t blocks = std::max<int64_t>((items + per_block - 1) / per_block, (M_cap + 31) / 32);
   static const int64_t cap = resident_blocks(quantize_1x128_kernel<true>, dev);
   if (blocks > cap) blocks = cap;
   quantize_1x128_kernel<true><<<static_cast<unsigned>(blocks), kQThreads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(M_cap), static_cast<uint32_t>(K / 128), ldx,
-      static_cast<uint8_t*>(q), ldq, sA, ld_sa, row_token);
+      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(T), static_cast<uint32_t>(K / 128), ldx,
+      static_cast<uint8_t*>(q), ldq, sA, ld_sa, entry_row, 0u, static_cast<uint32_t>(topk), row_token,
+      static_cast<uint32_t>(M_cap));
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 

@@ -25,17 +25,41 @@ def _tokens(T, K, seed):
 
 
 def _run(x, ids, E, m_cap=None):
-    q, sA, offs, rows = g.route_gather_quantize_1x128(x.cuda(), torch.from_numpy(ids).cuda(), E, m_cap)
+    q, sA, offs, rows, ent = g.route_gather_quantize_1x128(x.cuda(), torch.from_numpy(ids).cuda(), E, m_cap)
     torch.cuda.synchronize()
-    return q.cpu().numpy(), sa_from_device(sA, q.shape[0]), offs.cpu().numpy(), rows.cpu().numpy()
+    return (q.cpu().numpy(), sa_from_device(sA, q.shape[0]), offs.cpu().numpy(), rows.cpu().numpy(),
+            ent.cpu().numpy())
+
+
+def _entry_rows(ids, offs, E):
+    """The row of each (token, slot) entry under the layout rule: an expert's rows start at its
+    offset and are handed out in (token, slot) order; -1 for an id outside [0, E)."""
+    ent = np.full(ids.shape, -1, np.int32)
+    nxt = [int(o) for o in offs[:E]]
+    for t in range(ids.shape[0]):
+        for j in range(ids.shape[1]):
+            e = int(ids[t, j])
+            if 0 <= e < E:
+                ent[t, j] = nxt[e]
+                nxt[e] += 1
+    return ent
+
+
+def _check_entries(ent, ids, offs_r, rows_r, E):
+    want = _entry_rows(ids, offs_r, E)
+    valid = want >= 0
+    # the rule agrees with the oracle's row -> token map, and the library's map is that rule's
+    assert np.array_equal(rows_r[want[valid]], np.nonzero(valid)[0])
+    assert np.array_equal(ent, want)
 
 
 def _check(x, ids, E, m_cap=None):
-    q, sA, offs, rows = _run(x, ids, E, m_cap)
+    q, sA, offs, rows, ent = _run(x, ids, E, m_cap)
     check_status()
     q_r, s_r, offs_r, rows_r = route_gather_quantize(x.float().numpy(), ids, E, q.shape[0])
     assert np.array_equal(offs, offs_r)
     assert np.array_equal(rows, rows_r)
+    _check_entries(ent, ids, offs_r, rows_r, E)
     assert np.array_equal(q, q_r)
     assert np.array_equal(sA.view(np.uint32), s_r.view(np.uint32))
 
@@ -65,32 +89,34 @@ def test_a_token_naming_one_expert_twice_gets_two_rows():
 def test_no_tokens():
     x = torch.empty((0, 256), dtype=torch.bfloat16)
     ids = np.zeros((0, 2), dtype=np.int32)
-    q, sA, offs, rows = _run(x, ids, 4)
+    q, sA, offs, rows, ent = _run(x, ids, 4)
     check_status()
-    assert not offs.any() and np.all(rows == -1) and not q.any() and not sA.any()
+    assert not offs.any() and np.all(rows == -1) and not q.any() and not sA.any() and ent.size == 0
 
 
 def test_ids_out_of_range_are_dropped_and_flagged():
     x = _tokens(6, 128, 5)
     ids = np.array([[0, 7], [1, -1], [0, 1], [3, 2], [2, 0], [9, 1]], dtype=np.int32)
-    q, sA, offs, rows = _run(x, ids, 4)
+    q, sA, offs, rows, ent = _run(x, ids, 4)
     assert g.fp8g_get_status() == 6  # FP8G_ERR_DEVICE_ASSERT
     # the layout of the valid entries alone (out-of-range entries replaced by a fifth expert)
     ids5 = np.where((ids >= 0) & (ids < 4), ids, 4)
     offs5, rows5 = route_layout(ids5, 5)
     assert np.array_equal(offs, offs5[:5])
     assert np.array_equal(rows[:offs5[4]], rows5[:offs5[4]]) and np.all(rows[offs5[4]:] == -1)
+    assert np.array_equal(ent, _entry_rows(ids, offs5, 4))  # dropped entries: -1
 
 
 def test_full_size_moe_contiguous_layout():
     w = WORKLOADS["moe_contiguous"]
     inp = make_inputs(w, "cuda")
     ids = inp["topk_ids"].numpy()
-    q, sA, offs, rows = g.route_gather_quantize_1x128(inp["tokens"], inp["topk_ids"].cuda(), w.E)
+    q, sA, offs, rows, ent = g.route_gather_quantize_1x128(inp["tokens"], inp["topk_ids"].cuda(), w.E)
     torch.cuda.synchronize()
     check_status()
     offs_r, rows_r = route_layout(ids, w.E, q.shape[0])
     assert np.array_equal(offs.cpu().numpy(), offs_r) and np.array_equal(rows.cpu().numpy(), rows_r)
+    _check_entries(ent.cpu().numpy(), ids, offs_r, rows_r, w.E)
     # the rows equal the quantisation of the generator's gathered A, row for row
     m_total = inp["A"].shape[0]
     assert int(offs_r[-1]) == m_total
@@ -117,7 +143,7 @@ def test_routed_layout_feeds_the_contiguous_gemm():
     T, E, k, N, K = 260, 4, 2, 256, 512
     x = _tokens(T, K, 11)
     ids = _routing(T, E, k, 11)
-    q, sA, offs, rows = g.route_gather_quantize_1x128(x.cuda(), torch.from_numpy(ids).cuda(), E)
+    q, sA, offs, rows, _ = g.route_gather_quantize_1x128(x.cuda(), torch.from_numpy(ids).cuda(), E)
     gen = torch.Generator().manual_seed(12)
     Bq, sB = g.quantize_128x128((torch.randn((E, N, K), generator=gen) / np.sqrt(K)).to(torch.bfloat16).cuda())
     m_cap = q.shape[0]
