@@ -213,6 +213,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Programmatic dependent launch.  launch_dependents: the next kernel on the stream, if launched
+// with programmatic stream serialisation, may start now.  wait: block until the grids this one
+// depends on have completed and their memory is visible (returns at once without such a grid).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Register rebalancing between warpgroups (every thread of the warpgroup executes it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_release() {

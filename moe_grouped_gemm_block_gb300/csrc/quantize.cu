@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
         quant_n<16, FMT>(f, s, FMT == kE4M3 ? direct_mode(a, s) : 0u, c);
         const uint32_t m = it[u].m + row0;
         if constexpr (SCATTER) {
+          griddep_wait();  // the layout kernel's rows (at once after the first time)
           for (uint32_t j = 0; j < topk; ++j) {
             const int32_t r = __ldg(row_src + static_cast<int64_t>(m) * topk + j);
             if (r < 0) continue;
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
   }
   if constexpr (SCATTER) {
     // zero rows, a warp per row (the rows written above are all mapped, so none is written twice)
+    griddep_wait();
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t gwarp = (blockIdx.x * kQThreads + threadIdx.x) >> 5, nwarps = gridDim.x * (kQThreads / 32);
     for (uint32_t r = gwarp; r < rows_out; r += nwarps) {
@@ -482,6 +484,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_kernel(
   __shared__ int32_t s_warp[kRouteThreads / 32];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_launch_dependents();  // the quantiser may start loading tokens (it waits before its stores)
   for (int e = tid; e < E; e += kRouteThreads) s_count[e] = 0;
   if (tid == 0) s_bad = 0;
   __syncthreads();
@@ -574,9 +577,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
   constexpr int W = kRouteThreads / 32;
   __shared__ int32_t s_wcnt[W][kRouteSmallExperts];  // counts, then each warp's first rank
   __shared__ int32_t s_off[kRouteSmallExperts + 1];
+  __shared__ int32_t s_tot[kRouteSmallExperts];       // entries per expert
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < W * kRouteSmallExperts; i += kRouteThreads) (&s_wcnt[0][0])[i] = 0;
+  griddep_launch_dependents();  // the quantiser may start loading tokens (it waits before its stores)
+  for (int i = tid; i < W * E; i += kRouteThreads) s_wcnt[i / E][i % E] = 0;  // the counters in use
   if (tid == 0) s_bad = 0;
   __syncthreads();
   const int32_t L = (n + W - 1) / W;
@@ -603,14 +608,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
     else s_bad = 1;
   }
   __syncthreads();
-  if (tid < E) {  // per expert: exclusive scan over the warps, total in s_off (temporarily)
-    int32_t run = 0;
-    for (int w = 0; w < W; ++w) {
-      const int32_t c = s_wcnt[w][tid];
-      s_wcnt[w][tid] = run;
-      run += c;
+  static_assert(W == 32, "one lane per warp in the scan below");
+  for (int e = warp; e < E; e += W) {  // per expert (a warp each): exclusive scan over the warps
+    const int32_t c = s_wcnt[lane][e];
+    int32_t incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
     }
-    s_off[tid] = run;
+    s_wcnt[lane][e] = incl - c;
+    if (lane == 31) s_tot[e] = incl;
   }
   __syncthreads();
   if (warp == 0) {  // padded counts -> exclusive prefix (8 experts per lane)
@@ -619,7 +627,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
 #pragma unroll
     for (int j = 0; j < kRouteSmallExperts / 32; ++j) {
       const int e = lane * (kRouteSmallExperts / 32) + j;
-      v[j] = e < E ? (s_off[e] + 127) / 128 * 128 : 0;
+      v[j] = e < E ? (s_tot[e] + 127) / 128 * 128 : 0;
       local += v[j];
     }
     int32_t incl = local;
@@ -642,17 +650,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
   __syncthreads();
   const bool fits = static_cast<int64_t>(s_off[E]) <= M_cap;
   for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = fits ? s_off[e] : 0;
-  for (int64_t r = tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
-  if (!fits)
+  // token -1 for the padding rows only (every other row is written below): each group's rows past
+  // its entries, and the rows past the last group
+  if (fits) {
+    for (int e = 0; e < E; ++e)
+      for (int32_t r = s_off[e] + s_tot[e] + tid; r < s_off[e + 1]; r += kRouteThreads) row_token[r] = -1;
+    for (int64_t r = s_off[E] + tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
+  } else {
+    for (int64_t r = tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
     for (int32_t i = tid; i < n; i += kRouteThreads) entry_row[i] = -1;
-  __syncthreads();
+  }
   if (fits) {
     // 32 entries at a time (warp-uniform): lanes choosing the same expert take consecutive rows in
-    // lane order (match_any); the last of them advances the warp's count for that expert
-    auto assign = [&](int32_t b, int32_t e) {
+    // lane order (match_any); the last of them advances the warp's count for that expert.  The
+    // match_any of the cached chunks are independent and issued first; only the count updates run
+    // chunk after chunk.
+    auto assign = [&](int32_t b, int32_t e, unsigned peers) {
       const int32_t i = b + lane;
-      if (i >= hi || e < 0 || e >= E) e = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       if (e >= 0) {
         const int32_t r = s_off[e] + s_wcnt[warp][e] + rank;
@@ -665,12 +679,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_layout_small_kernel(
       if (e >= 0 && (peers >> lane) == 1u) s_wcnt[warp][e] += __popc(peers);
       __syncwarp();
     };
+    unsigned pe[kIdCache];
+#pragma unroll
+    for (int j = 0; j < kIdCache; ++j) {
+      const int32_t i = lo + 32 * j + lane;
+      if (i >= hi || idc[j] < 0 || idc[j] >= E) idc[j] = -1;
+      pe[j] = lo + 32 * j < hi ? __match_any_sync(0xffffffffu, idc[j]) : 0u;
+    }
 #pragma unroll
     for (int j = 0; j < kIdCache; ++j) {
       if (lo + 32 * j >= hi) break;
-      assign(lo + 32 * j, idc[j]);
+      assign(lo + 32 * j, idc[j], pe[j]);
     }
-    for (int32_t b = lo + 32 * kIdCache; b < hi; b += 32) assign(b, b + lane < hi ? __ldg(ids + b + lane) : -1);
+    for (int32_t b = lo + 32 * kIdCache; b < hi; b += 32) {
+      int32_t e = b + lane < hi ? __ldg(ids + b + lane) : -1;
+      if (e < 0 || e >= E) e = -1;
+      assign(b, e, __match_any_sync(0xffffffffu, e));
+    }
   }
   if (tid == 0 && (s_bad || !fits)) record_status(status, FP8G_ERR_DEVICE_ASSERT);
 }
@@ -812,11 +837,26 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
   int64_t blocks = std::max<int64_t>((items + per_block - 1) / per_block, (M_cap + 31) / 32);
   static const int64_t cap = resident_blocks(quantize_1x128_kernel<true>, dev);
   if (blocks > cap) blocks = cap;
-  quantize_1x128_kernel<true><<<static_cast<unsigned>(blocks), kQThreads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<uint32_t>(T), static_cast<uint32_t>(K / 128), ldx,
-      static_cast<uint8_t*>(q), ldq, sA, ld_sa, entry_row, 0u, static_cast<uint32_t>(topk), row_token,
-      static_cast<uint32_t>(M_cap));
-  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+  // launched as a programmatic dependent of the layout kernel: its CTAs start while the layout
+  // (one CTA) runs, load and quantise their first tokens, and wait for the layout before storing
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, quantize_1x128_kernel<true>, static_cast<const __nv_bfloat16*>(x),
+                         static_cast<uint32_t>(T), static_cast<uint32_t>(K / 128), ldx, static_cast<uint8_t*>(q), ldq,
+                         sA, ld_sa, static_cast<const int32_t*>(entry_row), 0u, static_cast<uint32_t>(topk),
+                         static_cast<const int32_t*>(row_token), static_cast<uint32_t>(M_cap)) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8G_ERR_CUDA;
+  }
+  return FP8G_OK;
 }
 
 extern "C" int fp8_quantize_per_row(const void* x, int64_t M, int64_t K, int64_t ldx, void* q,

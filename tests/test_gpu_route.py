@@ -76,6 +76,14 @@ def test_route_gather_quantize_small(T, E, k, K):
     _check(_tokens(T, K, T + E), _routing(T, E, k, T * E), E)
 
 
+@pytest.mark.parametrize("E", [8, 300])
+def test_many_entries(E):
+    # 66000 entries: 2063 per warp of the layout kernel for up to 256 experts, past the 512 ids it
+    # keeps in registers; 300 experts take the kernel for more
+    T, k, K = 33000, 2, 128
+    _check(_tokens(T, K, 77), _routing(T, E, k, 78 + E), E)
+
+
 def test_many_empty_experts_and_a_larger_capacity():
     ids = np.array([[2047], [5], [5], [2047], [0]], dtype=np.int32)
     _check(_tokens(5, 256, 3), ids, 2048, m_cap=g.route_capacity(5, 1, 2048) + 256)
