@@ -550,6 +550,10 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       tmem_relinquish();
     }
   }
+  // Everything above (barriers, TMEM, tensor-map prefetch) reads no input.  Launched as a
+  // programmatic dependent of the kernel before it on the stream (a quantiser writing A), the
+  // grid may have started early: wait for that kernel's results before the first input read.
+  griddep_wait();
   // pair tiles per expert (prefix over experts), after the group table
   int32_t* ptab = table + (a.E + 1);
   // Group tables (grouped modes), built by the first epilogue warp.
@@ -1353,8 +1357,23 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     }
     return FP8G_OK;
   }
-  kern<<<grid, C::kThreads, smem, stream>>>(tA, tB, tD, tSA, tSB, args);
-  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+  // a programmatic dependent launch: the CTAs may start while the previous kernel on the stream
+  // finishes (their prologue overlaps its tail) and wait for it before reading inputs
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, tSA, tSB, args) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8G_ERR_CUDA;
+  }
+  return FP8G_OK;
 }
 
 // Stream-K workspace: one per (device, stream), allocated on the first call that needs it and

@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_1x128_kernel(
     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sA, int64_t ld_sa,
     const int32_t* __restrict__ row_src, uint32_t cap = 0, uint32_t topk = 1,
     const int32_t* __restrict__ zero_src = nullptr, uint32_t rows_out = 0) {
+  griddep_launch_dependents();  // a GEMM launched after this may start its prologue
   const int sub = threadIdx.x & (kQLanes - 1);
   const uint32_t group = (blockIdx.x * kQThreads + threadIdx.x) / kQLanes;
   const uint32_t n_groups = gridDim.x * kQGroupsPerBlock;
