@@ -89,7 +89,7 @@ struct Cfg {
   static constexpr int kColGroups = BN / kEpiCols;       // warpgroups covering the tile's columns
   // Narrow tiles (few, long K loops: small-M shapes) split the K blocks between two sets of
   // promotion warps (even / odd K blocks), whose FP32 partial sums are added at the tile end.
-  static constexpr int kKSplit = (BN == 64 && !SWAP) ? 2 : 1;
+  static constexpr int kKSplit = ((BN == 64 || BN == 48) && !SWAP) ? 2 : 1;
   static constexpr int kEpiGroups = kColGroups * kKSplit;  // warpgroups of epilogue warps
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kStoreWarps = 4 * kColGroups;     // warps that write D
@@ -122,10 +122,14 @@ struct Cfg {
   static constexpr int kKPS = (SMALL || SWAP) ? 2 : 1;
   // (swapped tiles: 32 KB of weights and 16 KB of activations per stage)
   static constexpr int kStages =
-      SMALL ? 6 : (SWAP ? 4 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 5 : 6)))));
+      SMALL ? (BN == 48 ? 7 : 6) : (SWAP ? 4 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 5 : 6)))));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 3 at 160, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
+  // TMEM columns between buffers: BN, but 64 for the 48-wide tiles (each buffer then starts on a
+  // 64-column boundary, as in the 64-wide tiles)
+  static constexpr uint32_t kTmemStride = BN == 48 ? 64u : static_cast<uint32_t>(BN);
+  static_assert(kTmemBufs * kTmemStride <= 512, "TMEM buffers");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kABytes = kARows * BK;       // one K block of A
   static constexpr int kBRows = PAIR ? BN / 2 : BN;      // B rows this CTA loads
@@ -159,10 +163,11 @@ struct Cfg {
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
   static_assert(kOffScale % 128 == 0 && kScaleStage % 128 == 0 && kOffSbv % 16 == 0, "scale staging alignment");
-  static_assert(BN == 64 || BN == 128 || BN == 160 || BN == 192 || BN == 256, "BN");
+  static_assert(BN == 48 || BN == 64 || BN == 128 || BN == 160 || BN == 192 || BN == 256, "BN");
+  static_assert(BN != 48 || SMALL, "48-wide tiles: the small-M variant");
   static_assert((BN != 192 && BN != 160) || (!SMALL && !PAIR && !KG),
                 "160- and 192-wide tiles: single-CTA block-scaled forms");
-  static_assert(!SMALL || BN == 64, "small-M tiles are 64 wide");
+  static_assert(!SMALL || BN == 64 || BN == 48, "small-M tiles are 64 or 48 wide");
   static_assert(!SWAP || (BN == 64 && !SMALL && !PAIR && !KG), "swapped tiles: 64 token columns, single CTA");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
   static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
@@ -426,6 +431,7 @@ __device__ __forceinline__ void get_pair_tile(const GemmArgs& a, const int32_t* 
 // One TMEM load of 32 or 64 columns with its wait (tcgen05.ld 32x32b.x32 / .x64).
 __device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[32]) { tmem_ld32_sync(taddr, v); }
 __device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[64]) { tmem_ld64_sync(taddr, v); }
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, float (&v)[48]) { tmem_ld48_sync(taddr, v); }
 
 // Bounded wait on an mbarrier phase.  On timeout: flag the CTA, record the status.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmArgs& a,
@@ -729,7 +735,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           ++np;
           if (!(wait_bounded(tempty(b), tph ^ 1u, a, abort_flag))) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + b * BN;
+          const uint32_t d_tmem = tmem_base + b * C::kTmemStride;
           for (int32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++it) {
             const uint32_t s = it % S, ph = (it / S) & 1u;
             if (!(wait_bounded(full(s), ph, a, abort_flag))) { ok = false; break; }
@@ -772,7 +778,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
               tc_fence_after();
               const uint64_t ad = adesc0 + ((s * C::kStageABytes + j * C::kABytes) >> 4);
               const uint64_t bd = bdesc0 + ((s * C::kStageBBytes + j * C::kBBytes) >> 4);
-              const uint32_t d_tmem = tmem_base + b * BN;
+              const uint32_t d_tmem = tmem_base + b * C::kTmemStride;
               if constexpr (PAIR) {
 #pragma unroll
                 for (int k = 0; k < BK / 32; ++k)
@@ -837,7 +843,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
                 tmem_seen = mbar_test_wait(tempty(kn % NB), ((kn / NB) & 1u) ^ 1u);
                 const uint64_t ad = adesc0 + ((s * C::kStageABytes + j * C::kABytes) >> 4);
                 const uint64_t bd = bdesc0 + ((s * C::kStageBBytes + j * C::kBBytes) >> 4);
-                const uint32_t d_tmem = tmem_base + b * BN;
+                const uint32_t d_tmem = tmem_base + b * C::kTmemStride;
                 if constexpr (PAIR) {  // rank 0 issues for the pair; both CTAs' partials are ready
 #pragma unroll
                   for (int k = 0; k < BK / 32; ++k)
@@ -914,7 +920,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) { ok = false; break; }
         tc_fence_after();
         if (live) {
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * C::kTmemStride + col0;
 #pragma unroll
           for (int c = 0; c < C::kEpiCols / 64; ++c) {
             float v[64];
@@ -966,7 +972,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) return false;
           tc_fence_after();
           float v[NC];
-          tmem_ld32_sync(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0, v);
+          tmem_ld32_sync(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * C::kTmemStride + col0, v);
           tc_fence_before();
           __syncwarp();
           release_tmem(b);
@@ -997,22 +1003,29 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         const float* sap = a.sA + static_cast<int64_t>(ti.kb_first) * a.ld_sa + grow;
         const float* sbp = a.sB + (static_cast<int64_t>(ti.g) * a.NBs + ncol0 / 128) * a.KB;
         const bool blk_sb = MODE != kKGrouped && has_cols;
-        auto load_scales = [&](int32_t kbi, float& sa_o, float& sb_o) {
+        // 48-wide tiles may straddle a 128-column weight block: its columns from `cut` on take the
+        // next block's scale (cut is a multiple of 16, so a column pair never straddles it)
+        constexpr bool kTwoSb = C::kEpiCols == 48;
+        const int32_t cut = kTwoSb ? 128 - ncol0 % 128 : C::kEpiCols;
+        const bool has_hi = kTwoSb && cut < C::kEpiCols && ncol0 / 128 + 1 < a.NBs;
+        auto load_scales = [&](int32_t kbi, float& sa_o, float& sb_o, float& sbh_o) {
           sa_o = ld_nc_f32_or0(sap + static_cast<int64_t>(kbi) * a.ld_sa, MODE != kKGrouped && row_ok && kbi < pc.kb1);
           sb_o = ld_nc_f32_or0(sbp + kbi, blk_sb && kbi < pc.kb1);
+          sbh_o = kTwoSb ? ld_nc_f32_or0(sbp + a.KB + kbi, blk_sb && has_hi && kbi < pc.kb1) : 0.0f;
         };
-        float sa0, sb0, sa1, sb1;
-        load_scales(pc.kb0 + kpart, sa0, sb0);
-        load_scales(pc.kb0 + kpart + KS, sa1, sb1);
+        float sa0, sb0, sbh0, sa1, sb1, sbh1;
+        load_scales(pc.kb0 + kpart, sa0, sb0, sbh0);
+        load_scales(pc.kb0 + kpart + KS, sa1, sb1, sbh1);
         // What sets the pace of the wide tiles: a TMEM buffer is written again (K block kb + NB)
         // only after all of its warps have loaded it, so each K block's MMA, its completion, these
         // loads and the release form a chain that NB = 2 buffers must cover.
-        auto step = [&](int32_t kb, float& sa_r, float& sb_r) -> bool {
+        auto step = [&](int32_t kb, float& sa_r, float& sb_r, float& sbh_r) -> bool {
           const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
           const uint32_t b = it % NB, tph = (it / NB) & 1u;
           const uint32_t s = it % S, sph = (it / S) & 1u;  // (one K block per stage)
           float sa_kb = sa_r, sb_kb = sb_r;
-          load_scales(kb + 2 * KS, sa_r, sb_r);
+          const float sbh_kb = sbh_r;
+          load_scales(kb + 2 * KS, sa_r, sb_r, sbh_r);
           if constexpr (MODE == kKGrouped) {
             // the stage's scales land long before its partial: take them first
             if (!__all_sync(0xffffffffu, wait_bounded(sfull(s), sph, a, abort_flag))) return false;
@@ -1027,9 +1040,11 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           }
           const float scale = sa_kb * sb_kb;
           const float2 scale2 = make_float2(scale, scale);
+          const float scale_hi = sa_kb * sbh_kb;
+          const float2 scale2_hi = make_float2(scale_hi, scale_hi);
           if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) return false;
           tc_fence_after();
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN + col0;
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * C::kTmemStride + col0;
           if (live) {
             // this warp's columns in loads of kLd (one load and its wait each)
             constexpr int kLd = C::kEpiCols >= 64 ? 64 : C::kEpiCols;
@@ -1055,6 +1070,10 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
                   acc[c * 32 + 2 * i + 1] =
                       __ffma2_rn(make_float2(v[4 * i + 2], v[4 * i + 3]), s23, acc[c * 32 + 2 * i + 1]);
                 }
+              } else if constexpr (kTwoSb) {
+#pragma unroll
+                for (int i = 0; i < kLd / 2; ++i)
+                  acc[i] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), 2 * i < cut ? scale2 : scale2_hi, acc[i]);
               } else {
 #pragma unroll
                 for (int i = 0; i < kLd / 2; ++i)
@@ -1077,9 +1096,9 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           return true;
         };
         for (int32_t kb = pc.kb0 + kpart; kb < pc.kb1; kb += 2 * KS) {
-          if (!step(kb, sa0, sb0)) { ok = false; break; }
+          if (!step(kb, sa0, sb0, sbh0)) { ok = false; break; }
           if (kb + KS >= pc.kb1) break;
-          if (!step(kb + KS, sa1, sb1)) { ok = false; break; }
+          if (!step(kb + KS, sa1, sb1, sbh1)) { ok = false; break; }
         }
       }
       it_base += static_cast<uint32_t>(pc.kb1 - pc.kb0);
@@ -1183,7 +1202,8 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           for (int j = 0; j < C::kEpiCols / 2; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(sc, sc));
         }
       }
-      if ((MODE != kMasked && MODE != kKGrouped) || nvalid == 32) {
+      // (48-wide tiles take the plain stores: a 32-column box would spill into the next tile)
+      if (C::kEpiCols % 32 == 0 && ((MODE != kMasked && MODE != kKGrouped) || nvalid == 32)) {
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 32; ++j) {
           if (ncol0 + 32 * j >= a.N) break;
@@ -1212,8 +1232,8 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           }
         }
       } else if (lane < nvalid) {
-        // partial rows (a masked expert's count, the last rows of a K-grouped expert's matrix):
-        // plain stores, row by row
+        // partial rows (a masked expert's count, the last rows of a K-grouped expert's matrix, the
+        // small-M tiles' rows up to M) and 48-wide tiles: plain stores, row by row
         __nv_bfloat16* drow = a.D + static_cast<int64_t>(ti.d_row + q * 32 + lane) * a.ldd + ncol0;
 #pragma unroll
         for (int j = 0; j < C::kEpiCols / 8; ++j) {
@@ -1282,6 +1302,7 @@ constexpr int kMaxExperts160 = 512;
 static_assert(Cfg<160>::kOffTable + 4 * (kMaxExperts160 + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<64, true>::kOffTable <= kSmemLimit, "smem");
+static_assert(Cfg<48, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<64, false, false, false, true>::kOffTable <= kSmemLimit, "smem");
 static_assert(Cfg<256, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128, false, true>::kOffTable + 8 * (kMaxExperts + 1) <= kSmemLimit, "smem");
@@ -1473,7 +1494,8 @@ int env_pair() {
   return (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) ? e[0] - '0' : 0;
 }
 
-// FP8G_BLOCK_N (64, 128, 160, 192 or 256) forces the tile width; read on every call.  160 and 192
+// FP8G_BLOCK_N (48, 64, 128, 160, 192 or 256) forces the tile width; read on every call (48: decode
+// shapes only).  160 and 192
 // are only taken this way: measured slower than 256 on the large shapes (4096 x 8192 x 8192: 361 and
 // 288 us against 212).  Per K block a narrower tile still needs four tcgen05.mma, and one issuing
 // thread took ~620 cycles for the four N = 160 MMAs and their commit against ~325 cycles of MMA
@@ -1481,7 +1503,7 @@ int env_pair() {
 int env_block_n() {
   const char* e = std::getenv("FP8G_BLOCK_N");
   const int x = e ? std::atoi(e) : 0;
-  return (x == 64 || x == 128 || x == 160 || x == 192 || x == 256) ? x : 0;
+  return (x == 48 || x == 64 || x == 128 || x == 160 || x == 192 || x == 256) ? x : 0;
 }
 
 // Pick BN: fewest (waves x per-tile cost), the per-tile cost growing with BN plus a fixed
@@ -1540,7 +1562,13 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   // small-M variant (64-row A boxes)
   const bool swap = MODE == kDense && !EPI && o.rows <= 64 && env_block_n() == 0 && env_swap_ab();
   if (swap) bn = 64;
-  const bool small_m = MODE == kDense && !swap && bn == 64 && o.rows <= 64;
+  // Small-M tiles are 64 wide, or 48 with FP8G_BLOCK_N=48 (other shapes and forms have no 48-wide
+  // tiles).  On 64 x 7168 x 7168 the 150 48-wide tiles measured no faster than the 112 64-wide ones
+  // (25.2 us either way): each CTA still walks all 56 K blocks at the same ~590 cycles a block, and
+  // that serial loop, not the number of SMs streaming, sets the time.
+  const bool small_ok = MODE == kDense && !EPI && !swap && o.rows <= 64;
+  if (!small_ok && bn == 48) bn = 64;
+  const bool small_m = small_ok && (bn == 64 || bn == 48);
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
   // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2); the epilogue-scaled variant has single-CTA tiles
   const int pmode = (EPI || MODE == kKGrouped) ? 0 : env_pair();
@@ -1757,6 +1785,12 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
         }
         t_last_stages = Cfg<128>::kStages;
         return launch_kernel<128, MODE>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
+      case 48:
+        if constexpr (MODE == kDense) {
+          t_last_stages = Cfg<48, true>::kStages;
+          return launch_kernel<48, kDenseSmallM>(a, tA, tB, tD, tSA, tSB, grid, table_entries, stream);
+        }
+        return FP8G_ERR_INVALID_ARG;
       default:
         if constexpr (MODE == kDense) {
           if (small_m) {

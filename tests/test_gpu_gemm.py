@@ -57,6 +57,8 @@ def _dense_gpu(qa, sa, qb, sb, bn=None):
     (200, 208, 384, 160), (300, 592, 1024, 160), (513, 400, 640, 160), (257, 1024, 640, 160),
     (64, 1792, 7168, 64), (257, 1024, 640, 256), (513, 384, 256, None),
     (40, 256, 384, 64), (17, 128, 1152, 64),  # small M, odd K-block counts (part-filled stages)
+    # 48-wide small-M tiles: tiles straddling a 128-column weight-scale block, N tails, odd K blocks
+    (1, 16, 128, 48), (40, 256, 384, 48), (17, 208, 1152, 48), (64, 1792, 7168, 48), (64, 7168, 2048, 48),
 ])
 def test_dense_small_shapes(M, N, K, bn):
     qa, sa, qb, sb = _problem(M, N, K, seed=M * 7 + N + K)
