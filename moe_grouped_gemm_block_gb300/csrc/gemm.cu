@@ -130,6 +130,14 @@ struct Cfg {
   // 64-column boundary, as in the 64-wide tiles)
   static constexpr uint32_t kTmemStride = BN == 48 ? 64u : static_cast<uint32_t>(BN);
   static_assert(kTmemBufs * kTmemStride <= 512, "TMEM buffers");
+  // Small-M tiles synchronise the MMA and the promotion once per stage, not once per K block:
+  // a stage's kKPS partials go to one TMEM slot of kKPS buffers, completed by one commit, and the
+  // slot is written again once every promotion warp (both K parts) has read its K block of it.
+  // The lone issuers' barrier round trips (~100-200 cycles each) otherwise set the pace of these
+  // short MMAs.
+  static constexpr bool kStageSync = SMALL;
+  static constexpr uint32_t kSlotCols = kStageSync ? static_cast<uint32_t>(kKPS) * kTmemStride : kTmemStride;
+  static constexpr uint32_t kTmemSlots = kStageSync ? 512u / kSlotCols : static_cast<uint32_t>(kTmemBufs);
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kABytes = kARows * BK;       // one K block of A
   static constexpr int kBRows = PAIR ? BN / 2 : BN;      // B rows this CTA loads
@@ -171,6 +179,8 @@ struct Cfg {
   static_assert(!SWAP || (BN == 64 && !SMALL && !PAIR && !KG), "swapped tiles: 64 token columns, single CTA");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
   static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
+  static_assert(!kStageSync || (kKSplit == 2 && kKPS == 2 && kMmaWarps == 2),
+                "stage-synchronised tiles: K part j reads K block j of every stage, two lone issuers");
 };
 
 // The configuration of a kernel instantiation.
@@ -526,11 +536,12 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       mbar_init(empty(s), kEmptyArrivals);
       mbar_init(sfull(s), 1);  // the producer's expect-tx arrival
     }
-    // each TMEM buffer is consumed by the warps of one K part
+    // each TMEM buffer is consumed by the warps of one K part (a stage-synchronised slot: by
+    // every promotion warp)
     for (uint32_t b = 0; b < NB; ++b) {
       mbar_init(tfull(b), 1);
       // in a pair, the promotion warps of both CTAs release rank 0's buffer
-      mbar_init(tempty(b), PAIR ? 2 * C::kStoreWarps : C::kStoreWarps);
+      mbar_init(tempty(b), C::kStageSync ? C::kEpiWarps : (PAIR ? 2 * C::kStoreWarps : C::kStoreWarps));
     }
     mbar_init(xfull, C::kStoreWarps);
     mbar_init(xempty, C::kStoreWarps);
@@ -817,7 +828,45 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         bool full_seen = false, tmem_seen = false;  // early tests for the next own K block
         Work w = make_work(num_tiles, tile_step, tile0, a.KB, false, 0, 0);  // whole tiles
         Piece pc;
-        while (ok && next_piece(w, pc)) {
+        if constexpr (C::kStageSync) {
+          // stage `it` fills TMEM slot it % NSL (its K block j in buffer j of the slot): one wait
+          // for the slot, one commit for its partials, one for the operand stage
+          constexpr uint32_t NSL = C::kTmemSlots;
+          while (ok && next_piece(w, pc)) {
+            Tile ti;
+            if (!fetch_tile(pc, ti)) continue;
+            for (int32_t kb0 = 0; kb0 < a.KB; kb0 += KPS, ++it) {
+              if (it % MW != mi) continue;
+              const int32_t left = a.KB - kb0;
+              const uint32_t nk = static_cast<uint32_t>(left < KPS ? left : KPS);
+              const uint32_t s = it % S, ph = (it / S) & 1u;
+              const uint32_t sl = it % NSL, tph = (it / NSL) & 1u;
+              if (!wait_seen(full_seen, full(s), ph, a, abort_flag)) { ok = false; break; }
+              if (!wait_seen(tmem_seen, tempty(sl), tph ^ 1u, a, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              // test the next own stage's barriers now; the MMAs below hide the round trips.  Neither
+              // test can take an older phase for this one: stage nx - S was filled before stage it,
+              // and the release of stage nx - 2 NSL came before that of stage it - NSL, awaited above.
+              const uint32_t nx = it + MW;
+              full_seen = mbar_test_wait(full(nx % S), (nx / S) & 1u);
+              tmem_seen = mbar_test_wait(tempty(nx % NSL), ((nx / NSL) & 1u) ^ 1u);
+              for (uint32_t j = 0; j < nk; ++j) {
+                const uint64_t ad = adesc0 + ((s * C::kStageABytes + j * C::kABytes) >> 4);
+                const uint64_t bd = bdesc0 + ((s * C::kStageBBytes + j * C::kBBytes) >> 4);
+                const uint32_t d_tmem = tmem_base + sl * C::kSlotCols + j * C::kTmemStride;
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k)
+                  mma_f8f6f4(true, d_tmem, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+              }
+              mma_commit(true, tfull(sl));
+              mma_commit(true, empty(s));  // the stage is free once these MMAs have read it
+              issued = true;
+              last_bar = tfull(sl);
+              last_ph = tph;
+            }
+          }
+        }
+        while (!C::kStageSync && ok && next_piece(w, pc)) {
           Tile ti;
           if (!fetch_tile(pc, ti)) continue;
           for (int32_t kb0 = 0; kb0 < a.KB && ok; kb0 += KPS, ++it) {
@@ -895,6 +944,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
     const uint32_t sbv_addr = base + C::kOffSbv + ew * 512u;  // K-grouped: this warp's B scales
     float2* xbuf = reinterpret_cast<float2*>(smem + C::kOffX);
     uint32_t it_base = 0, tiles_done = 0;
+    uint32_t st_base = 0;  // stages of earlier pieces (stage-synchronised TMEM slots)
     uint32_t np = 0;  // pieces taken (EPI: the TMEM buffer sequence, as the MMA warp counts it)
     bool ok = true;
     // stream-K workspace slot of this thread: float4 j of thread e sits at slot[j * kEpiThreads + e]
@@ -1021,7 +1071,15 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         // loads and the release form a chain that NB = 2 buffers must cover.
         auto step = [&](int32_t kb, float& sa_r, float& sb_r, float& sbh_r) -> bool {
           const uint32_t it = it_base + static_cast<uint32_t>(kb - pc.kb0);
-          const uint32_t b = it % NB, tph = (it / NB) & 1u;
+          // the barrier pair, its phase and the TMEM columns of this K block's partial
+          uint32_t b = it % NB, tph = (it / NB) & 1u, tcol = b * C::kTmemStride;
+          if constexpr (C::kStageSync) {
+            const uint32_t r = static_cast<uint32_t>(kb - pc.kb0);
+            const uint32_t st = st_base + r / C::kKPS;
+            b = st % C::kTmemSlots;
+            tph = (st / C::kTmemSlots) & 1u;
+            tcol = b * C::kSlotCols + (r % C::kKPS) * C::kTmemStride;
+          }
           const uint32_t s = it % S, sph = (it / S) & 1u;  // (one K block per stage)
           float sa_kb = sa_r, sb_kb = sb_r;
           const float sbh_kb = sbh_r;
@@ -1044,7 +1102,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           const float2 scale2_hi = make_float2(scale_hi, scale_hi);
           if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), tph, a, abort_flag))) return false;
           tc_fence_after();
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * C::kTmemStride + col0;
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + tcol + col0;
           if (live) {
             // this warp's columns in loads of kLd (one load and its wait each)
             constexpr int kLd = C::kEpiCols >= 64 ? 64 : C::kEpiCols;
@@ -1100,8 +1158,25 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           if (kb + KS >= pc.kb1) break;
           if (!step(kb + KS, sa1, sb1, sbh1)) { ok = false; break; }
         }
+        if constexpr (C::kStageSync) {
+          // a last stage holding fewer K blocks than K parts: the warps of the K parts without
+          // one release its slot too, once its partials have been written (so that the release
+          // is counted in that phase, not an earlier one)
+          const int32_t n = pc.kb1 - pc.kb0;
+          if (ok && n % C::kKPS != 0 && kpart >= n % C::kKPS) {
+            const uint32_t st = st_base + static_cast<uint32_t>(n - 1) / C::kKPS;
+            const uint32_t b = st % C::kTmemSlots;
+            if (!__all_sync(0xffffffffu, wait_bounded(tfull(b), (st / C::kTmemSlots) & 1u, a, abort_flag))) {
+              ok = false;
+            } else {
+              __syncwarp();
+              release_tmem(b);
+            }
+          }
+        }
       }
       it_base += static_cast<uint32_t>(pc.kb1 - pc.kb0);
+      st_base += static_cast<uint32_t>(pc.kb1 - pc.kb0 + C::kKPS - 1) / C::kKPS;
       if (!ok) break;
       if constexpr (C::kKSplit > 1) {
         // add the odd-K-block partial sums (second warpgroup) into the first warpgroup's
