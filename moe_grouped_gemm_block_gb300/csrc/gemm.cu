@@ -93,13 +93,14 @@ struct Cfg {
   static constexpr int kEpiGroups = kColGroups * kKSplit;  // warpgroups of epilogue warps
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kStoreWarps = 4 * kColGroups;     // warps that write D
-  // MMA issuing threads (lane 0 of warps 1 .. kMmaWarps), taking alternate pipeline stages.
+  // MMA issuing threads (lane 0 of warps 1 .. kMmaWarps), taking the pipeline stages in turn.
   // One thread pays ~60 cycles per tcgen05.mma plus ~170 per mbarrier round trip, which caps
-  // the narrow small-M tiles (whose MMAs are short); there two issuers share the stream.
-  // Wider tiles keep one: their MMAs are long enough, and measured slower with two.
+  // the narrow small-M tiles (whose MMAs are short); there three issuers share the stream (one:
+  // 22.6 us for 64 x 7168 x 7168, two: 17.4, three: 16.8).  Wider tiles keep one: their MMAs
+  // are long enough, and measured slower with two.
   // 256 x 128 pair tiles: four MMAs of ~64 cycles per K block for the pair, so two lone issuers;
   // 160-wide tiles: four MMAs of ~81 cycles per K block, also two.
-  static constexpr int kMmaWarps = (SMALL || (PAIR && BN == 128) || BN == 160) ? 2 : 1;
+  static constexpr int kMmaWarps = SMALL ? 3 : (((PAIR && BN == 128) || BN == 160) ? 2 : 1);
   // BN = 256, 192 and 160: a full first warpgroup (producer / MMA / idle) then the epilogue
   // warpgroups, so that setmaxnreg can move registers to the epilogue.  BN = 256: the launch gives
   // 384 x 168 = 64512, rebalanced to 128 x 40 + 256 x 232 = 64512.  BN = 192: 512 x 128 = 65536,
@@ -121,8 +122,9 @@ struct Cfg {
   // pieces of rows 7 KB apart reaches about half the bandwidth of 256-byte runs.
   static constexpr int kKPS = (SMALL || SWAP) ? 2 : 1;
   // (swapped tiles: 32 KB of weights and 16 KB of activations per stage)
+  // (a multiple of the lone issuers' count: see the assertion below)
   static constexpr int kStages =
-      SMALL ? (BN == 48 ? 7 : 6) : (SWAP ? 4 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 5 : 6)))));
+      SMALL ? 6 : (SWAP ? 4 : (PAIR ? (BN == 256 ? 5 : 8) : (KG ? 3 : (BN >= 192 ? 4 : (BN == 160 ? 4 : 6)))));
   // TMEM partial buffers: as many as fit the 512 columns, so the MMA can run ahead of the
   // promotion by several K blocks (2 at BN = 256, 3 at 160, 4 at 128, 8 at 64).
   static constexpr int kTmemBufs = 512 / BN > 8 ? 8 : 512 / BN;
@@ -179,8 +181,13 @@ struct Cfg {
   static_assert(!SWAP || (BN == 64 && !SMALL && !PAIR && !KG), "swapped tiles: 64 token columns, single CTA");
   static_assert(!PAIR || ((BN == 256 || BN == 128) && !SMALL), "CTA pairs use 128- or 256-wide tiles");
   static_assert(kEpiWarp0 > kMmaWarps, "producer and MMA warps precede the epilogue");
-  static_assert(!kStageSync || (kKSplit == 2 && kKPS == 2 && kMmaWarps == 2),
-                "stage-synchronised tiles: K part j reads K block j of every stage, two lone issuers");
+  // Lone issuers wait for a stage's operands by the parity of its full barrier's phase, which is
+  // only sound if the stage's previous fill (kStages stages earlier) has landed.  Copies may land
+  // out of order, so an issuer knows that only of the stages it consumed itself: each stage slot
+  // must always go to the same issuer.
+  static_assert(kMmaWarps == 1 || kStages % kMmaWarps == 0, "lone issuers: one issuer per stage slot");
+  static_assert(!kStageSync || (kKSplit == 2 && kKPS == 2 && kMmaWarps >= 2),
+                "stage-synchronised tiles: K part j reads K block j of every stage, lone issuers");
 };
 
 // The configuration of a kernel instantiation.
@@ -820,7 +827,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         // CTA's tiles) holds the K blocks kb0 .. kb0 + nk - 1 of its tile, nk = min(KPS, K blocks
         // left); `kit` counts the K blocks of all earlier stages (the TMEM buffer sequence, as
         // the epilogue counts them).
-        static_assert(MW == 2, "two lone issuers");
+        static_assert(MW == 2 || C::kStageSync, "two lone issuers (stage-synchronised tiles: any number)");
         const uint32_t mi = static_cast<uint32_t>(warp - 1);
         uint32_t it = 0, kit = 0;
         bool ok = true, issued = false;
@@ -1371,7 +1378,7 @@ constexpr uint32_t kSmemLimit = 232448;  // 227 KB: the per-block dynamic shared
 static_assert(Cfg<256>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<128>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
 static_assert(Cfg<192>::kOffTable + 4 * (kMaxExperts + 1) <= kSmemLimit, "smem");
-// 160-wide tiles (five 36 KB stages and twenty 2 KB staging boxes) leave room for the group tables
+// 160-wide tiles (four 36 KB stages and twenty 2 KB staging boxes) leave room for the group tables
 // of up to 512 experts; grouped calls with more experts take 256-wide tiles.
 constexpr int kMaxExperts160 = 512;
 static_assert(Cfg<160>::kOffTable + 4 * (kMaxExperts160 + 1) <= kSmemLimit, "smem");

@@ -66,7 +66,7 @@ def _dgrad_problem(M, N, K, seed):
 
 @pytest.mark.parametrize("M,N,K,bn", [
     (128, 256, 512, None), (200, 208, 384, 256), (200, 208, 384, 128), (129, 272, 256, 64),
-    (64, 1792, 2048, None),  # the small-M variant (two lone issuers)
+    (64, 1792, 2048, None),  # the small-M variant (lone issuers)
     (17, 128, 1152, 64),
     (513, 384, 256, None),
 ])
