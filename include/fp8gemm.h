@@ -19,7 +19,7 @@
  *                  fp8_quantize_1x128_e5m2, fp8_gemm_nt_dgrad, fp8_grouped_gemm_contiguous_dgrad,
  *                  fp8_grouped_gemm_wgrad
  *   status         fp8g_get_status, fp8g_status_string, fp8g_selftest_bounded_waits, fp8g_last_config,
- *                  fp8g_last_split, fp8g_last_swap_ab
+ *                  fp8g_last_split, fp8g_last_swap_ab, fp8g_last_cluster_k
  *
  * Sources (page title, section):
  *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
@@ -437,6 +437,19 @@ int fp8g_last_split(int* split);
  * FP8G_ERR_INVALID_ARG for a null pointer.
  */
 int fp8g_last_swap_ab(int* swapped);
+
+/*
+ * fp8g_last_cluster_k -- the cluster size c when the last GEMM call on this thread split each
+ * 256-wide tile's K blocks over a cluster of c CTAs, else 0.  A block-scaled dense GEMM
+ * (fp8_gemm_nt, fp8_gemm_nt_dgrad) with few tiles: rank r of a cluster promotes K blocks
+ * [r KB / c, (r+1) KB / c) and rank 0 adds the other ranks' FP32 partials before rounding once
+ * ("DeepGEMM FP8 walk-through" sec. 2.3: FP32 accumulation over the whole K, one rounding on
+ * write; sec. 3.2: work spread over the SMs from the shape).  Same results up to FP32 summation
+ * order.  Opt-in: FP8G_CLUSTER_K=c (2 .. 8), taken when the tiles times c fit the SMs and c
+ * divides the K blocks (at least two a rank).  Diagnostic only; returns FP8G_OK, or
+ * FP8G_ERR_INVALID_ARG for a null pointer.
+ */
+int fp8g_last_cluster_k(int* ck);
 
 #ifdef __cplusplus
 }

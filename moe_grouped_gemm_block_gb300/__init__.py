@@ -78,6 +78,7 @@ _SIGNATURES = {
     "fp8g_last_config": [ctypes.POINTER(ctypes.c_int)] * 3,
     "fp8g_last_split": [ctypes.POINTER(ctypes.c_int)],
     "fp8g_last_swap_ab": [ctypes.POINTER(ctypes.c_int)],
+    "fp8g_last_cluster_k": [ctypes.POINTER(ctypes.c_int)],
 }
 
 
@@ -403,14 +404,17 @@ def fp8g_get_status(stream: torch.cuda.Stream | None = None) -> int:
 
 
 def fp8g_last_config() -> dict:
-    """Tile width, stages, grid, whether the tail was split (stream-K) and whether the tiles were swapped
-    (decode shapes: weight rows on the MMA's M) in this thread's last GEMM."""
+    """Tile width, stages, grid, whether the tail was split (stream-K), whether the tiles were swapped
+    (decode shapes: weight rows on the MMA's M) and the cluster size of a cluster K split (0: none) in
+    this thread's last GEMM."""
     bn, st, gr, sp, sw = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    ck = ctypes.c_int()
     _check(lib().fp8g_last_config(ctypes.byref(bn), ctypes.byref(st), ctypes.byref(gr)), "fp8g_last_config")
     _check(lib().fp8g_last_split(ctypes.byref(sp)), "fp8g_last_split")
     _check(lib().fp8g_last_swap_ab(ctypes.byref(sw)), "fp8g_last_swap_ab")
+    _check(lib().fp8g_last_cluster_k(ctypes.byref(ck)), "fp8g_last_cluster_k")
     return {"block_n": bn.value, "stages": st.value, "grid": gr.value, "split": bool(sp.value),
-            "swap_ab": bool(sw.value)}
+            "swap_ab": bool(sw.value), "cluster_k": ck.value}
 
 
 # ------------------------------------------------------------------ allocating wrappers

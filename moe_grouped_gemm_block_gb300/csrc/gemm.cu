@@ -168,7 +168,7 @@ struct Cfg {
   static constexpr uint32_t kOffSbv = kOffScale + kStages * kScaleStage;
   static constexpr uint32_t kOffX = kOffSbv + kSbvBytes;
   static constexpr uint32_t kOffBar = kOffX + kXBytes;
-  static constexpr uint32_t kNumBars = 3 * kStages + 2 * kTmemBufs + 4;
+  static constexpr uint32_t kNumBars = 3 * kStages + 2 * kTmemBufs + 5;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
@@ -223,6 +223,9 @@ struct GemmArgs {
   int32_t sk_min_gain;  // split only when it saves at least this many K blocks per CTA
   float4* ws_part;
   uint32_t* ws_flag;
+  // cluster K split (see make_work), 0 or 1 when off: each cluster of ck CTAs computes one tile,
+  // its ranks taking consecutive K ranges; rank 0 adds the others' partials (workspace slots)
+  int32_t ck;
 
   // Test hook, -1 normally: the producer never fills its stage number `test_skip_stage` (counted
   // over the CTA's stages), so the MMA issuer's bounded wait for it runs out and the abort path
@@ -258,13 +261,26 @@ struct Work {
   int32_t tail0, u;           // first tail tile, tail K blocks per CTA
   int32_t unit, unit_end;     // this CTA's tail units
 };
+// Cluster K split (ck > 1; dense single-CTA tiles, one tile per cluster, ck dividing KB): the
+// stream-K tail with no whole tiles and u = KB / ck, so that CTA c is rank c % ck of cluster c / ck
+// and takes K blocks [(c % ck) u, (c % ck + 1) u) of tile c / ck.  Rank 0 finishes the tile with the
+// partials of ranks 1 .. ck-1 (CTAs c+1 .. c+ck-1), which signal it through its shared memory: no
+// flags to clear, and the cluster launch makes the ranks resident together.
 __device__ __forceinline__ Work make_work(int32_t num_tiles, int32_t G, int32_t c, int32_t KB, bool sk,
-                                          int32_t min_units, int32_t min_gain) {
+                                          int32_t min_units, int32_t min_gain, int32_t ck = 0) {
   Work w;
   w.G = G;
   w.KB = KB;
   w.c = c;
   w.t = c;
+  if (ck > 1) {
+    w.t = w.t_end = w.tail0 = 0;
+    w.u = KB / ck;
+    const int64_t U = static_cast<int64_t>(num_tiles) * KB, s0 = static_cast<int64_t>(c) * w.u;
+    w.unit = static_cast<int32_t>(s0 < U ? s0 : U);
+    w.unit_end = static_cast<int32_t>(s0 + w.u < U ? s0 + w.u : U);
+    return w;
+  }
   if (!sk) {
     w.t_end = num_tiles;
     w.tail0 = num_tiles;
@@ -525,6 +541,10 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
   const uint32_t sk_ready = xfull + 24u;    // stream-K: the partials to add are complete
   // the scales of stage s have landed (K-grouped form)
   auto sfull = [&](uint32_t st) { return xfull + 32u + 8u * st; };
+  // cluster K split: the partials of the other ranks are written (rank 0's barrier, ck - 1 arrivals)
+  // (both recomputed from the kernel parameters where used, rather than kept in registers)
+  auto ck_in = [&]() { return xfull + 32u + 8u * S; };
+  auto ck_on = [&]() { return MODE == kDense && !PAIR && !EPI && a.ck > 1; };
   constexpr bool kStaged = MODE == kKGrouped;
   // Arrivals that free an operand stage: the MMA commit (lone issuers, CTA pairs and the
   // epilogue-scaled variant); else one lane of the promotion warps once the stage's MMAs have
@@ -554,6 +574,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
     mbar_init(xempty, C::kStoreWarps);
     mbar_init(sk_written, C::kEpiWarps);
     mbar_init(sk_ready, 1);
+    mbar_init(ck_in(), ck_on() ? static_cast<uint32_t>(a.ck - 1) : 1u);
     misc[1] = 0;
     misc[2] = 0;  // set when the group table is out of contract
     fence_mbar_init();
@@ -642,6 +663,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) cluster_sync();  // the peer's barriers and TMEM exist before any signalling
+  if (ck_on()) cluster_sync();         // rank 0's barrier exists before the other ranks signal it
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
 
@@ -685,7 +707,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       uint32_t it = 0;  // stages filled
       bool ok = true;
       bool empty_seen = false;  // early test of the next stage's empty barrier (lone form)
-      Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+      Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain, ck_on() ? a.ck : 0);
       Piece pc;
       while (ok && next_piece(w, pc)) {
         Tile ti;
@@ -744,7 +766,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         // a K block's MMAs frees its stage, the commit after the last one hands the buffer over
         uint32_t it = 0, np = 0;
         bool ok = true;
-        Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+        Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain, ck_on() ? a.ck : 0);
         Piece pc;
         while (ok && next_piece(w, pc)) {
           Tile ti;
@@ -779,7 +801,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         // left in it)); `kit` counts K blocks, the TMEM buffer sequence as the epilogue counts it
         uint32_t it = 0, kit = 0;
         bool ok = true;
-        Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+        Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain, ck_on() ? a.ck : 0);
         Piece pc;
         while (ok && next_piece(w, pc)) {
           Tile ti;
@@ -958,7 +980,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
     constexpr int kEpiThreads = C::kEpiWarps * 32;
     constexpr int64_t kSlotF4 = static_cast<int64_t>(kEpiThreads) * (C::kEpiCols / 4);
     const int e_thr = ew * 32 + lane;
-    Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain);
+    Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain, ck_on() ? a.ck : 0);
     Piece pc;
     while (ok && next_piece(w, pc)) {
       Tile ti;
@@ -1214,28 +1236,41 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       if (pc.kind == kContrib) {
         // part of a split tile: the FP32 partial goes to this CTA's workspace slot (L2), then
         // the flag is raised once every epilogue warp has written its share
+        // (warps whose rows are all past the matrix skip it, and the finishing CTA skips them too)
         float4* slot = a.ws_part + static_cast<int64_t>(blockIdx.x) * kSlotF4;
+        if (ti.a_row + q * 32 < a.rows) {
 #pragma unroll
-        for (int j = 0; j < C::kEpiCols / 4; ++j)
-          __stcg(slot + static_cast<int64_t>(j) * kEpiThreads + e_thr,
-                 make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y));
+          for (int j = 0; j < C::kEpiCols / 4; ++j)
+            __stcg(slot + static_cast<int64_t>(j) * kEpiThreads + e_thr,
+                   make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y));
+        }
         __threadfence();
         __syncwarp();
         if (lane == 0) mbar_arrive(sk_written);
-        if (ew == 0 && lane == 0 && wait_bounded(sk_written, 0u, a, abort_flag))
-          st_release_gpu(a.ws_flag + blockIdx.x, 1u);
+        if (ew == 0 && lane == 0 && wait_bounded(sk_written, 0u, a, abort_flag)) {
+          if (ck_on()) {  // signal rank 0 of the cluster (release at cluster scope)
+            fence_acq_rel_cluster();
+            mbar_arrive_remote(mapa_shared(ck_in(), 0));
+          } else {
+            st_release_gpu(a.ws_flag + blockIdx.x, 1u);
+          }
+        }
         continue;
       }
       if (pc.kind == kFinish) {
         // first K blocks of a split tile: add the partials of CTAs c_lo .. c_hi once their
         // flags are up (one thread waits; it releases the others even on a timeout)
         if (ew == 0 && lane == 0) {
-          bool got = true;
-          for (int32_t c2 = pc.c_lo; c2 <= pc.c_hi && got; ++c2) got = wait_flag(a.ws_flag + c2, a, abort_flag);
+          if (ck_on()) {
+            if (wait_bounded(ck_in(), 0u, a, abort_flag)) fence_acq_rel_cluster();
+          } else {
+            bool got = true;
+            for (int32_t c2 = pc.c_lo; c2 <= pc.c_hi && got; ++c2) got = wait_flag(a.ws_flag + c2, a, abort_flag);
+          }
           mbar_arrive(sk_ready);
         }
         if (!__all_sync(0xffffffffu, wait_bounded(sk_ready, 0u, a, abort_flag))) { ok = false; break; }
-        for (int32_t c2 = pc.c_lo; c2 <= pc.c_hi; ++c2) {
+        for (int32_t c2 = pc.c_lo; c2 <= pc.c_hi && ti.a_row + q * 32 < a.rows; ++c2) {
           const float4* slot = a.ws_part + static_cast<int64_t>(c2) * kSlotF4;
 #pragma unroll
           for (int j = 0; j < C::kEpiCols / 4; ++j) {
@@ -1336,6 +1371,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
+  if (ck_on()) cluster_sync();         // rank 0 leaves after every rank has signalled it
   tc_fence_after();
   if (warp == 1) {
     if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
@@ -1431,6 +1467,27 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tD, tSA, tSB, args) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8G_ERR_CUDA;
+    }
+    return FP8G_OK;
+  }
+  if (args.ck > 1) {
+    // cluster K split: clusters of ck CTAs (the grid is a multiple of ck), co-scheduled, so that
+    // rank 0's wait for the other ranks' partials always ends
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(args.ck);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -1559,6 +1616,13 @@ bool env_swap_ab() {
   const char* e = std::getenv("FP8G_SWAP_AB");
   return e && e[0] == '1' && e[1] == 0;
 }
+// FP8G_CLUSTER_K=c (2 .. 8) splits the K blocks of each 256-wide tile of a dense block-scaled call
+// over a cluster of c CTAs when the tiles are few (read on every call; 0 otherwise).
+int env_cluster_k() {
+  const char* e = std::getenv("FP8G_CLUSTER_K");
+  if (!e || e[0] < '2' || e[0] > '8' || e[1] != 0) return 0;
+  return e[0] - '0';
+}
 
 // FP8G_STREAMK=0 turns the stream-K tail off (read on every call).
 bool env_streamk() {
@@ -1567,6 +1631,7 @@ bool env_streamk() {
 }
 
 thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0, t_last_split = 0, t_last_swap = 0;
+thread_local int t_last_ck = 0;
 
 // FP8G_PAIR=1 runs 256-wide tiles as 256 x 256 CTA-pair tiles, FP8G_PAIR=2 as 256 x 128 pair
 // tiles (four TMEM partial buffers per CTA).  Off by default: measured no faster than single-CTA
@@ -1644,6 +1709,9 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   // small-M variant (64-row A boxes)
   const bool swap = MODE == kDense && !EPI && o.rows <= 64 && env_block_n() == 0 && env_swap_ab();
   if (swap) bn = 64;
+  // cluster K split (opt-in): 256-wide single-CTA tiles, each computed by a cluster of CTAs
+  const int ck_req = (MODE == kDense && !EPI && !swap && !no_alloc) ? env_cluster_k() : 0;
+  if (ck_req > 1) bn = 256;
   // Small-M tiles are 64 wide, or 48 with FP8G_BLOCK_N=48 (other shapes and forms have no 48-wide
   // tiles).  On 64 x 7168 x 7168 the 150 48-wide tiles measured no faster than the 112 64-wide ones
   // (25.2 us either way): each CTA still walks all 56 K blocks at the same ~590 cycles a block, and
@@ -1654,7 +1722,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   // 256-wide tiles run as CTA pairs unless there are too few rows: 256 x 256 pair tiles
   // (FP8G_PAIR=1) or 256 x 128 (FP8G_PAIR=2); the epilogue-scaled variant has single-CTA tiles
   const int pmode = (EPI || MODE == kKGrouped) ? 0 : env_pair();
-  const bool pair = bn == 256 && pmode != 0 &&
+  const bool pair = bn == 256 && pmode != 0 && ck_req <= 1 &&
                     (MODE != kDense || (o.rows + BM - 1) / BM >= 2) && dev->sm_count >= 2;
   if (pair && pmode == 2) bn = 128;
 
@@ -1787,7 +1855,19 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   };
   // (160-wide tiles have two MMA issuers, which take whole tiles; swapped tiles split too: their
   // N / 128 weight slabs are fewer than the SMs)
-  if (MODE != kKGrouped && !pair && !small_m && (swap || (bn >= 128 && bn != 160)) && env_streamk() &&
+  // cluster K split: every tile gets a cluster of ck CTAs when they all fit on the SMs at once and
+  // ck divides the K blocks, at least two a rank (the clusters wait only within themselves)
+  a.ck = 0;
+  if (ck_req > 1 && !pair && static_cast<int64_t>(a.num_tiles) * ck_req <= dev->sm_count && a.KB % ck_req == 0 &&
+      a.KB >= 2 * ck_req) {
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    if (sk_workspace(dev_id, dev->sm_count, stream, &a.ws_part, &a.ws_flag)) {
+      a.ck = ck_req;
+      grid = a.num_tiles * ck_req;
+    }
+  }
+  if (a.ck <= 1 && MODE != kKGrouped && !pair && !small_m && (swap || (bn >= 128 && bn != 160)) && env_streamk() &&
       (MODE == kMasked || tail_splits(a.num_tiles))) {
     int dev_id = 0;
     cudaGetDevice(&dev_id);
@@ -1822,6 +1902,7 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   t_last_bn = bn;
   t_last_grid = grid;
   t_last_split = a.sk;
+  t_last_ck = a.ck;
   t_last_swap = swap ? 1 : 0;
   if constexpr (MODE == kKGrouped) {
     if (bn == 256) {
@@ -2112,6 +2193,12 @@ extern "C" int fp8g_last_split(int* split) {
 extern "C" int fp8g_last_swap_ab(int* swapped) {
   if (!swapped) return FP8G_ERR_INVALID_ARG;
   *swapped = t_last_swap;
+  return FP8G_OK;
+}
+
+extern "C" int fp8g_last_cluster_k(int* ck) {
+  if (!ck) return FP8G_ERR_INVALID_ARG;
+  *ck = t_last_ck;
   return FP8G_OK;
 }
 

@@ -270,6 +270,9 @@ __device__ __forceinline__ void cluster_sync() {
 }
 // Arrive on an mbarrier of a peer CTA (cluster address).  Default (CTA-scope) semantics: the
 // caller orders what must precede it (tcgen05.fence::before_thread_sync for TMEM reads).
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }

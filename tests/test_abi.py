@@ -103,6 +103,7 @@ def test_last_config_null_pointer(lib):
     assert lib.fp8g_last_config(null, null, null) == INVALID
     assert lib.fp8g_last_split(null) == INVALID
     assert lib.fp8g_last_swap_ab(null) == INVALID
+    assert lib.fp8g_last_cluster_k(null) == INVALID
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):

@@ -16,7 +16,7 @@ import torch
 import moe_grouped_gemm_block_gb300 as g
 from moe_grouped_gemm_block_gb300.workloads import WORKLOADS, make_inputs
 from tests import oracle_jobs
-from tests.gpu_util import assert_gemm_close, bf16_to_np, check_status, need_gpu, sa_from_device
+from tests.gpu_util import assert_gemm_close, bf16_to_np, check_status, env_var, need_gpu, sa_from_device
 
 pytestmark = pytest.mark.gpu
 SENTINEL = 0x7FC1  # a bf16 NaN bit pattern no GEMM produces
@@ -58,8 +58,10 @@ def _assert_codes(q_gpu, s_gpu, q_ref, s_ref, what):
     assert np.array_equal(s_gpu.view(np.uint32), s_ref.view(np.uint32)), f"{what}: scales differ from the oracle"
 
 
-@pytest.mark.parametrize("name", ["decode", "large_4096", "large_4096x8192"])
-def test_dense_full_size_every_element(ex, name):
+@pytest.mark.parametrize("name,ck", [("decode", None), ("decode", "4"), ("large_4096", None),
+                                     ("large_4096x8192", None)])
+def test_dense_full_size_every_element(ex, name, ck):
+    # ck: the cluster K split (FP8G_CLUSTER_K), 28 tiles of 256 columns x 4 ranks on the decode shape
     need_gpu()
     w = WORKLOADS[name]
     inp = make_inputs(w, "cuda")
@@ -67,8 +69,10 @@ def test_dense_full_size_every_element(ex, name):
     qA, sA = g.quantize_1x128(A)
     qB, sB = g.quantize_128x128(B)
     D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
-    g.fp8_gemm_nt(qA, sA, qB, sB, D)
-    torch.cuda.synchronize()
+    with env_var("FP8G_CLUSTER_K", ck):
+        g.fp8_gemm_nt(qA, sA, qB, sB, D)
+        torch.cuda.synchronize()
+        assert g.fp8g_last_config()["cluster_k"] == (int(ck) if ck else 0)
     check_status()
     qa, sa = _oracle_acts(ex, A.float().cpu().numpy())
     qb, sb = _oracle_weights(ex, B.float().cpu().numpy())

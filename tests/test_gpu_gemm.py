@@ -131,6 +131,28 @@ def test_dense_swapped_decode_tiles(M, N, K, split):
     assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"swapped {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K,ck,want", [
+    (64, 1024, 1024, 2, 2),    # 4 tiles, 4 K blocks a rank
+    (64, 1792, 2048, 4, 4),
+    (40, 768, 1024, 4, 4),     # two K blocks a rank
+    (128, 512, 2048, 8, 8),    # eight ranks
+    (1, 256, 512, 2, 2),
+    (200, 512, 1024, 2, 2),    # two m-blocks, ragged M
+    (100, 2304, 4096, 4, 4),   # ragged N (9 tiles)
+    (64, 1024, 1152, 4, 0),    # 9 K blocks: 4 does not divide them, no split
+])
+def test_dense_cluster_k_split(M, N, K, ck, want):
+    # FP8G_CLUSTER_K: each 256-wide tile's K blocks split over a cluster of CTAs, rank 0 adding the
+    # other ranks' FP32 partials before the one rounding
+    qa, sa, qb, sb = _problem(M, N, K, seed=7 * M + N + K)
+    with env_var("FP8G_CLUSTER_K", str(ck)):
+        D = _dense_gpu(qa, sa, qb, sb)
+        cfg = g.fp8g_last_config()
+    check_status()
+    assert cfg["cluster_k"] == want, cfg
+    assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"cluster K split {M}x{N}x{K} ck={ck}")
+
+
 def test_dense_swapped_tiles_switch_and_strides():
     # by default M <= 64 takes the 64-wide small-M tiles; strided operands and ld_sa > M in the
     # swapped form (FP8G_SWAP_AB=1)
