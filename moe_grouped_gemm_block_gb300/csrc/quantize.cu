@@ -370,9 +370,11 @@ __global__ void __launch_bounds__(256) quantize_128x128_kernel(
 // ("DeepGEMM FP8 walk-through" sec. 2.2); same scale and code rules as the block forms.
 
 // One CTA per row.  The row's 16-byte pieces are held in registers (rows of up to
-// kRowThreads * kRowVec * 8 values) between the amax reduction and the quantisation; longer
-// rows read the rest again (from L1 / L2).
-constexpr int kRowThreads = 256;
+// kRowThreads * kRowVec * 8 = 8192 values) between the amax reduction and the quantisation; longer
+// rows read the rest again (from L1 / L2).  128 threads a row: with ~80 registers a thread, six
+// rows (96 KB at K = 8192) are in flight per SM, against three rows of half the loads a thread
+// with 256 threads a row (4096 x 8192: 32.7 us).
+constexpr int kRowThreads = 128;
 constexpr int kRowVec = 8;
 
 __device__ __forceinline__ float block_amax(float a, float* red) {
@@ -438,18 +440,46 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(
 // the value order, and RN(a / 448) is non-decreasing in a, so the largest of the CTAs' values is
 // RN(amax / 448) of the whole tensor.  s[e] starts at +0.
 constexpr int kTensorThreads = 256;
+constexpr int kTensorUnroll = 8;  // independent 16-byte loads in flight per thread
+
+// A thread's pieces (8 values) of tensor e: p, p + S, p + 2S, ... of the tensor's M x kvec pieces
+// (row-major), as (row, piece) pairs stepped without a division per piece.
+struct PieceWalk {
+  uint32_t r, v, sr, sv;
+  __device__ __forceinline__ PieceWalk(uint32_t p, uint32_t S, uint32_t kvec)
+      : r(p / kvec), v(p - (p / kvec) * kvec), sr(S / kvec), sv(S - (S / kvec) * kvec) {}
+  __device__ __forceinline__ void step(uint32_t kvec) {
+    r += sr;
+    v += sv;
+    if (v >= kvec) {
+      v -= kvec;
+      ++r;
+    }
+  }
+};
 
 __global__ void __launch_bounds__(kTensorThreads) tensor_scale_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t kvec, int64_t ldx, float* __restrict__ s) {
   __shared__ float red[kTensorThreads / 32];
+  griddep_launch_dependents();  // pass 2 may start loading its pieces (it waits before reading s)
   const uint32_t e = blockIdx.y;
-  const uint32_t total = M * kvec;  // the host guarantees M * K / 8 < 2^31
+  const __nv_bfloat16* xe = x + static_cast<int64_t>(e) * M * ldx;
   float a = 0.0f;
-  for (uint32_t p = blockIdx.x * kTensorThreads + threadIdx.x; p < total; p += gridDim.x * kTensorThreads) {
-    const uint32_t r = p / kvec, v = p - r * kvec;
-    float f[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(x + (static_cast<int64_t>(e) * M + r) * ldx) + v), f);
-    a = fmaxf(a, amax8(f));
+  PieceWalk w(blockIdx.x * kTensorThreads + threadIdx.x, gridDim.x * kTensorThreads, kvec);
+  while (w.r < M) {
+    uint4 raw[kTensorUnroll];
+#pragma unroll
+    for (int u = 0; u < kTensorUnroll; ++u) {
+      raw[u] = w.r < M ? __ldg(reinterpret_cast<const uint4*>(xe + static_cast<int64_t>(w.r) * ldx) + w.v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      w.step(kvec);
+    }
+#pragma unroll
+    for (int u = 0; u < kTensorUnroll; ++u) {
+      float f[8];
+      unpack8(raw[u], f);
+      a = fmaxf(a, amax8(f));
+    }
   }
   const float amax = block_amax(a, red);
   if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(s) + e, __float_as_uint(__fdiv_rn(amax, kE4M3Max)));
@@ -459,20 +489,45 @@ __global__ void __launch_bounds__(kTensorThreads) tensor_scale_kernel(
 // bf16 significand, recovered from s: for s normal, s * 448 is within 2^-23 (relative) of amax,
 // far inside half a bf16 step, so rounding it to bf16 gives amax back.  (For s subnormal or zero
 // the test is not used.)
+//
+// Launched as a programmatic dependent of pass 1: its CTAs may start while pass 1 runs and load
+// their first pieces (the input is not pass 1's output), then wait for pass 1 before reading s.
 __global__ void __launch_bounds__(kTensorThreads) quantize_tensor_kernel(
     const __nv_bfloat16* __restrict__ x, uint32_t M, uint32_t kvec, int64_t ldx, uint8_t* __restrict__ q,
     int64_t ldq, const float* __restrict__ s_in) {
   const uint32_t e = blockIdx.y;
-  const float s = __ldg(s_in + e);
-  const float amax = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s, kE4M3Max)));
-  const uint32_t direct = direct_mode(amax, s);
-  const uint32_t total = M * kvec;
-  for (uint32_t p = blockIdx.x * kTensorThreads + threadIdx.x; p < total; p += gridDim.x * kTensorThreads) {
-    const uint32_t r = p / kvec, v = p - r * kvec;
-    const int64_t row = static_cast<int64_t>(e) * M + r;
-    float f[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(x + row * ldx) + v), f);
-    reinterpret_cast<uint2*>(q + row * ldq)[v] = quant8(f, s, direct);
+  const __nv_bfloat16* xe = x + static_cast<int64_t>(e) * M * ldx;
+  uint8_t* qe = q + static_cast<int64_t>(e) * M * ldq;
+  PieceWalk w(blockIdx.x * kTensorThreads + threadIdx.x, gridDim.x * kTensorThreads, kvec);
+  bool first = true;
+  float s = 0.0f;
+  uint32_t direct = 0;
+  while (w.r < M) {
+    uint4 raw[kTensorUnroll];
+    uint32_t rr[kTensorUnroll], vv[kTensorUnroll];
+#pragma unroll
+    for (int u = 0; u < kTensorUnroll; ++u) {
+      rr[u] = w.r;
+      vv[u] = w.v;
+      raw[u] = w.r < M ? __ldg(reinterpret_cast<const uint4*>(xe + static_cast<int64_t>(w.r) * ldx) + w.v)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      w.step(kvec);
+    }
+    if (first) {  // pass 1's scale, once its grid has finished
+      first = false;
+      griddep_wait();
+      s = __ldcg(s_in + e);  // (written by pass 1 while this grid may already run: not the read-only path)
+      const float amax = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s, kE4M3Max)));
+      direct = direct_mode(amax, s);
+    }
+#pragma unroll
+    for (int u = 0; u < kTensorUnroll; ++u) {
+      if (rr[u] < M) {
+        float f[8];
+        unpack8(raw[u], f);
+        reinterpret_cast<uint2*>(qe + static_cast<int64_t>(rr[u]) * ldq)[vv[u]] = quant8(f, s, direct);
+      }
+    }
   }
 }
 
@@ -917,10 +972,24 @@ extern "C" int fp8_quantize_per_tensor(const void* x, int64_t E, int64_t M, int6
   tensor_scale_kernel<<<grid, kTensorThreads, 0, cs>>>(static_cast<const __nv_bfloat16*>(x),
                                                        static_cast<uint32_t>(M), kvec, ldx, s);
   if (cudaGetLastError() != cudaSuccess) return FP8G_ERR_CUDA;
-  quantize_tensor_kernel<<<grid, kTensorThreads, 0, cs>>>(static_cast<const __nv_bfloat16*>(x),
-                                                          static_cast<uint32_t>(M), kvec, ldx,
-                                                          static_cast<uint8_t*>(q), ldq, s);
-  return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
+  // pass 2 as a programmatic dependent of pass 1 (it waits for pass 1 before reading s)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTensorThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, quantize_tensor_kernel, static_cast<const __nv_bfloat16*>(x),
+                         static_cast<uint32_t>(M), kvec, ldx, static_cast<uint8_t*>(q), ldq,
+                         static_cast<const float*>(s)) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8G_ERR_CUDA;
+  }
+  return FP8G_OK;
 }
 
 extern "C" int fp8_quantize_128x128(const void* w, int64_t E, int64_t N, int64_t K, void* q,
