@@ -874,8 +874,10 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
               if (!wait_seen(tmem_seen, tempty(sl), tph ^ 1u, a, abort_flag)) { ok = false; break; }
               tc_fence_after();
               // test the next own stage's barriers now; the MMAs below hide the round trips.  Neither
-              // test can take an older phase for this one: stage nx - S was filled before stage it,
-              // and the release of stage nx - 2 NSL came before that of stage it - NSL, awaited above.
+              // test can take an older phase for this one: stage nx - S is this issuer's own (S is a
+              // multiple of MW) and already consumed, so its fill has landed; and every warp releases
+              // stages in order, so the release of stage nx - 2 NSL came before that of stage
+              // it - NSL, awaited above.
               const uint32_t nx = it + MW;
               full_seen = mbar_test_wait(full(nx % S), (nx / S) & 1u);
               tmem_seen = mbar_test_wait(tempty(nx % NSL), ((nx / NSL) & 1u) ^ 1u);
@@ -1235,7 +1237,8 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       }
       if (pc.kind == kContrib) {
         // part of a split tile: the FP32 partial goes to this CTA's workspace slot (L2), then
-        // the flag is raised once every epilogue warp has written its share
+        // the flag is raised once every epilogue warp has written its share (cluster K split:
+        // rank 0's barrier is signalled instead)
         // (warps whose rows are all past the matrix skip it, and the finishing CTA skips them too)
         float4* slot = a.ws_part + static_cast<int64_t>(blockIdx.x) * kSlotF4;
         if (ti.a_row + q * 32 < a.rows) {
@@ -1259,7 +1262,8 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       }
       if (pc.kind == kFinish) {
         // first K blocks of a split tile: add the partials of CTAs c_lo .. c_hi once their
-        // flags are up (one thread waits; it releases the others even on a timeout)
+        // flags are up, or (cluster K split) once they have signalled this CTA's barrier (one
+        // thread waits; it releases the others even on a timeout)
         if (ew == 0 && lane == 0) {
           if (ck_on()) {
             if (wait_bounded(ck_in(), 0u, a, abort_flag)) fence_acq_rel_cluster();
