@@ -7,6 +7,8 @@ shape is compared on sampled rows and column blocks after checking that the GPU'
 equal the oracle's there.
 """
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -80,6 +82,30 @@ def test_per_tensor_quantiser_bit_exact(shape):
         q_ref, s_ref = quantize_per_tensor(xs[e])
         assert np.array_equal(q.cpu().numpy().reshape(xs.shape)[e], q_ref), e
         assert s.cpu().numpy()[e].view(np.uint32) == s_ref[0].view(np.uint32), e
+
+
+@pytest.mark.parametrize("E,M,K", [(1, 37, 384), (3, 37, 384), (2, 130, 1024)])
+def test_per_tensor_strided_c_abi(E, M, K):
+    # row strides past K on both sides (through the C ABI; the binding takes contiguous tensors):
+    # the codes land in the first K bytes of each row, the rest of each row is left alone
+    ldx, ldq = K + 72, K + 48
+    x_full = _draw((E * M, ldx), seed=E * M + K, std=1.3)
+    x_full[:, K:] = 1e30  # outside the rows' K values: must not reach any amax
+    q_full = torch.full((E * M, ldq), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.empty(E, dtype=torch.float32, device="cuda")
+    xd = x_full.cuda()
+    rc = g.lib().fp8_quantize_per_tensor(ctypes.c_void_p(xd.data_ptr()), E, M, K, ldx, ctypes.c_void_p(q_full.data_ptr()),
+                                         ldq, ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    check_status()
+    xs = x_full[:, :K].float().numpy().reshape(E, M, K)
+    q = q_full.cpu().numpy()
+    for e in range(E):
+        q_ref, s_ref = quantize_per_tensor(xs[e])
+        assert np.array_equal(q[e * M:(e + 1) * M, :K], q_ref), e
+        assert s.cpu().numpy()[e].view(np.uint32) == s_ref[0].view(np.uint32), e
+    assert np.all(q[:, K:] == 0xAB)
 
 
 def test_per_tensor_zero_and_empty():
