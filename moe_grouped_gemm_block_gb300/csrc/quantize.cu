@@ -868,6 +868,157 @@ extern "C" int fp8_quantize_1x128_e5m2(const void* x, int64_t M, int64_t K, int6
   return cudaGetLastError() == cudaSuccess ? FP8G_OK : FP8G_ERR_CUDA;
 }
 
+// The same layout computed by several CTAs (at most 32 experts, the routing of a batch of
+// tokens).  Entry i of expert e goes to row offsets[e] + (entries of e before i), exactly as in
+// the one-CTA kernels above; CTA c assigns the entries [c C, (c+1) C) only.  Every CTA counts all
+// entries (n ids, from L2): the totals give the same padded offsets in each CTA, and the counts
+// before its range its rows' base.  Then its 32 warps take one slice of its range each.  The
+// one-CTA kernel's row assignment walked 256 entries a warp for 8192 entries; here a warp walks
+// n / (32 G).  8192 entries of 8 experts: 7.1 us against 11.6 (ncu), and the call with its
+// quantiser 35.5 against 36.9 us.  (The quantiser waits for the layout before its first store,
+// so only the layout's own time comes off.)
+constexpr int kRouteChunkExperts = 32;
+constexpr int kRouteChunkCtas = 8;
+constexpr int32_t kRouteChunkMinEntries = 2048;  // smaller layouts keep the one-CTA kernel
+
+__global__ void __launch_bounds__(kRouteThreads) route_layout_chunked_kernel(
+    const int32_t* __restrict__ ids, int32_t n, int32_t topk, int32_t E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_token, int32_t* __restrict__ entry_row, int64_t M_cap, unsigned int* status) {
+  constexpr int W = kRouteThreads / 32;
+  constexpr int XE = kRouteChunkExperts;
+  __shared__ int32_t s_all[W][XE];   // per warp: entries of each expert (all of them)
+  __shared__ int32_t s_pre[W][XE];   // per warp: entries of each expert before this CTA's range
+  __shared__ int32_t s_wcnt[W][XE];  // this CTA's warps: counts in their slices, then their first ranks
+  __shared__ int32_t s_tot[XE], s_base[XE], s_off[XE + 1];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_launch_dependents();  // the quantiser may start loading tokens (it waits before its stores)
+  const int32_t C = (n + static_cast<int32_t>(gridDim.x) - 1) / static_cast<int32_t>(gridDim.x);
+  const int32_t clo = min(n, static_cast<int32_t>(blockIdx.x) * C), chi = min(n, clo + C);
+  for (int i = tid; i < W * XE; i += kRouteThreads) {
+    (&s_all[0][0])[i] = 0;
+    (&s_pre[0][0])[i] = 0;
+    (&s_wcnt[0][0])[i] = 0;
+  }
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  // eight ids a thread loaded at once, then counted (one load latency per pass, not eight)
+  constexpr int kIdBatch = 8;
+  for (int32_t b0 = 0; b0 < n; b0 += kIdBatch * kRouteThreads) {
+    int32_t ev[kIdBatch];
+#pragma unroll
+    for (int j = 0; j < kIdBatch; ++j) {
+      const int32_t i = b0 + j * kRouteThreads + tid;
+      ev[j] = i < n ? __ldg(ids + i) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kIdBatch; ++j) {
+      const int32_t i = b0 + j * kRouteThreads + tid;
+      if (i >= n) continue;
+      if (ev[j] >= 0 && ev[j] < E) {
+        atomicAdd(&s_all[warp][ev[j]], 1);
+        if (i < clo) atomicAdd(&s_pre[warp][ev[j]], 1);
+      } else {
+        s_bad = 1;
+      }
+    }
+  }
+  // this CTA's range: warp w takes the slice [lo, hi); its first kIdCache * 32 ids stay in registers
+  // for the row assignment
+  const int32_t L = (chi - clo + W - 1) / W;
+  const int32_t lo = min(chi, clo + warp * L), hi = min(chi, lo + L);
+  constexpr int kIdCache = 4;
+  int32_t idc[kIdCache];
+#pragma unroll
+  for (int j = 0; j < kIdCache; ++j) {
+    const int32_t i = lo + 32 * j + lane;
+    idc[j] = i < hi ? __ldg(ids + i) : -1;
+    if (idc[j] < 0 || idc[j] >= E) idc[j] = -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kIdCache; ++j)
+    if (idc[j] >= 0) atomicAdd(&s_wcnt[warp][idc[j]], 1);
+  for (int32_t i = lo + 32 * kIdCache + lane; i < hi; i += 32) {
+    const int32_t e = __ldg(ids + i);
+    if (e >= 0 && e < E) atomicAdd(&s_wcnt[warp][e], 1);
+  }
+  __syncthreads();
+  static_assert(W == 32 && XE <= 32, "one lane per warp and per expert below");
+  for (int e = warp; e < E; e += W) {  // per expert (a warp each): sums and the scan over the warps
+    const int32_t c = s_wcnt[lane][e];
+    int32_t incl = c, all = s_all[lane][e], pre = s_pre[lane][e];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      all += __shfl_xor_sync(0xffffffffu, all, off);
+      pre += __shfl_xor_sync(0xffffffffu, pre, off);
+    }
+    s_wcnt[lane][e] = incl - c;
+    if (lane == 0) {
+      s_tot[e] = all;
+      s_base[e] = pre;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // padded counts -> exclusive prefix, one expert a lane
+    const int32_t v = lane < E ? (s_tot[lane] + 127) / 128 * 128 : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += u;
+    }
+    if (lane < E) s_off[lane] = incl - v;
+    if (lane == 31) s_off[E] = incl;
+  }
+  __syncthreads();
+  const bool fits = static_cast<int64_t>(s_off[E]) <= M_cap;
+  if (blockIdx.x == 0) {
+    for (int e = tid; e <= E; e += kRouteThreads) offsets[e] = fits ? s_off[e] : 0;
+    if (fits) {  // token -1 for the padding rows only (every other row is written below)
+      for (int e = 0; e < E; ++e)
+        for (int32_t r = s_off[e] + s_tot[e] + tid; r < s_off[e + 1]; r += kRouteThreads) row_token[r] = -1;
+      for (int64_t r = s_off[E] + tid; r < M_cap; r += kRouteThreads) row_token[r] = -1;
+    }
+    if (tid == 0 && (s_bad || !fits)) record_status(status, FP8G_ERR_DEVICE_ASSERT);
+  }
+  if (!fits) {  // an empty layout: every row padding, every entry dropped
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kRouteThreads;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kRouteThreads + tid; r < M_cap; r += stride) row_token[r] = -1;
+    for (int32_t i = clo + tid; i < chi; i += kRouteThreads) entry_row[i] = -1;
+    return;
+  }
+  // 32 entries at a time: lanes choosing the same expert take consecutive rows in lane order
+  for (int32_t b = lo, j = 0; b < hi; b += 32, ++j) {
+    const int32_t i = b + lane;
+    int32_t e = -1;
+    if (j < kIdCache) {
+#pragma unroll
+      for (int u = 0; u < kIdCache; ++u)
+        if (u == j) e = idc[u];
+    } else {
+      e = i < hi ? __ldg(ids + i) : -1;
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0) {
+      const int32_t r = s_off[e] + s_base[e] + s_wcnt[warp][e] + rank;
+      row_token[r] = i / topk;
+      entry_row[i] = r;
+    } else if (i < hi) {
+      entry_row[i] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && (peers >> lane) == 1u) s_wcnt[warp][e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t K, int64_t ldx,
                                                const int32_t* topk_ids, int32_t topk, int32_t E,
                                                void* q, int64_t ldq, float* sA, int64_t ld_sa,
@@ -891,7 +1042,11 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
   int st = current_device(&dev);
   if (st != FP8G_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (E <= kRouteSmallExperts)
+  if (E <= kRouteChunkExperts && n >= kRouteChunkMinEntries) {
+    const int64_t layout_ctas = std::min<int64_t>(kRouteChunkCtas, (n + 1023) / 1024);
+    route_layout_chunked_kernel<<<static_cast<unsigned>(layout_ctas), kRouteThreads, 0, s>>>(
+        topk_ids, static_cast<int32_t>(n), topk, E, group_offsets, row_token, entry_row, M_cap, dev->status);
+  } else if (E <= kRouteSmallExperts)
     route_layout_small_kernel<<<1, kRouteThreads, 0, s>>>(topk_ids, static_cast<int32_t>(n), topk, E,
                                                           group_offsets, row_token, entry_row, M_cap,
                                                           dev->status);
@@ -906,7 +1061,7 @@ extern "C" int fp8_route_gather_quantize_1x128(const void* x, int64_t T, int64_t
   static const int64_t cap = resident_blocks(quantize_1x128_kernel<true>, dev);
   if (blocks > cap) blocks = cap;
   // launched as a programmatic dependent of the layout kernel: its CTAs start while the layout
-  // (one CTA) runs, load and quantise their first tokens, and wait for the layout before storing
+  // runs, load and quantise their first tokens, and wait for the layout before storing
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kQThreads);
