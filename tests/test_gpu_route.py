@@ -115,6 +115,27 @@ def test_ids_out_of_range_are_dropped_and_flagged():
     assert np.array_equal(ent, _entry_rows(ids, offs5, 4))  # dropped entries: -1
 
 
+@pytest.mark.parametrize("T,E,k", [(1111, 8, 2), (1500, 32, 2), (4097, 5, 1), (2048, 1, 1)])
+def test_layout_over_several_ctas(T, E, k):
+    # 2048 entries or more of at most 32 experts: the layout kernel over several CTAs (uneven
+    # ranges and warp slices of fewer than 32 entries included); the same layout as the oracle's
+    _check(_tokens(T, 128, T + 11 * E), _routing(T, E, k, 5 * T + E), E)
+
+
+def test_layout_over_several_ctas_drops_ids_out_of_range():
+    T, E = 1200, 6
+    ids = _routing(T, E, 2, 99)
+    ids[7, 1], ids[400, 0], ids[1199, 1], ids[0, 0] = -3, 6, 1000, -1
+    x = _tokens(T, 128, 12)
+    q, sA, offs, rows, ent = _run(x, ids, E)
+    assert g.fp8g_get_status() == 6  # FP8G_ERR_DEVICE_ASSERT
+    ids7 = np.where((ids >= 0) & (ids < E), ids, E)
+    offs7, rows7 = route_layout(ids7, E + 1)
+    assert np.array_equal(offs, offs7[:E + 1])
+    assert np.array_equal(rows[:offs7[E]], rows7[:offs7[E]]) and np.all(rows[offs7[E]:] == -1)
+    assert np.array_equal(ent, _entry_rows(ids, offs7, E))
+
+
 def test_full_size_moe_contiguous_layout():
     w = WORKLOADS["moe_contiguous"]
     inp = make_inputs(w, "cuda")
