@@ -445,9 +445,11 @@ int fp8g_last_swap_ab(int* swapped);
  * [r KB / c, (r+1) KB / c) and rank 0 adds the other ranks' FP32 partials before rounding once
  * ("DeepGEMM FP8 walk-through" sec. 2.3: FP32 accumulation over the whole K, one rounding on
  * write; sec. 3.2: work spread over the SMs from the shape).  Same results up to FP32 summation
- * order.  Opt-in: FP8G_CLUSTER_K=c (2 .. 8), taken when the tiles times c fit the SMs and c
- * divides the K blocks (at least two a rank).  Diagnostic only; returns FP8G_OK, or
- * FP8G_ERR_INVALID_ARG for a null pointer.
+ * order.  Taken by default when M > 64, K has 128 blocks or more and the 256-wide tiles fill at
+ * most half the SMs (the largest c of 8, 4, 2 whose tiles fit the SMs, dividing the K blocks and
+ * leaving each rank 16 or more); FP8G_CLUSTER_K=c (2 .. 8) forces c where the tiles times c fit the
+ * SMs and c divides the K blocks (at least two a rank), FP8G_CLUSTER_K=0 turns it off.
+ * Diagnostic only; returns FP8G_OK, or FP8G_ERR_INVALID_ARG for a null pointer.
  */
 int fp8g_last_cluster_k(int* ck);
 

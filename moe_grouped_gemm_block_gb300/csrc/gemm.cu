@@ -1620,12 +1620,28 @@ bool env_swap_ab() {
   const char* e = std::getenv("FP8G_SWAP_AB");
   return e && e[0] == '1' && e[1] == 0;
 }
-// FP8G_CLUSTER_K=c (2 .. 8) splits the K blocks of each 256-wide tile of a dense block-scaled call
-// over a cluster of c CTAs when the tiles are few (read on every call; 0 otherwise).
+// FP8G_CLUSTER_K=c (2 .. 8) forces the cluster K split with clusters of c CTAs where it applies,
+// FP8G_CLUSTER_K=0 turns it off (read on every call); -1 when unset: the split is then chosen by
+// cluster_k_auto.
 int env_cluster_k() {
   const char* e = std::getenv("FP8G_CLUSTER_K");
-  if (!e || e[0] < '2' || e[0] > '8' || e[1] != 0) return 0;
+  if (!e) return -1;
+  if (e[0] == '0' && e[1] == 0) return 0;
+  if (e[0] < '2' || e[0] > '8' || e[1] != 0) return -1;
   return e[0] - '0';
+}
+
+// The cluster K split by default: for dense block-scaled calls with few 256-wide tiles (at most half
+// the SMs) and a long K (128 K blocks or more), the largest cluster of 8, 4 or 2 CTAs whose tiles
+// fit on the SMs, that divides the K blocks and leaves each rank 16 or more.  Measured (device time):
+// 128 x 1024 x 16384 41.7 -> 26.6 us, 128 x 2048 x 32768 80.9 -> 38.9, 512 x 1536 x 16384 43.0 ->
+// 32.7; with 64 K blocks (256 x 2048 x 8192) it did not pay, nor for 64 rows or fewer (the small-M
+// tiles, 64 x 4096 x 16384: 28.8 against 32.8 us).
+int cluster_k_auto(int64_t tiles256, int64_t KB, int sm_count) {
+  if (KB < 128 || tiles256 < 1 || 2 * tiles256 > sm_count) return 0;
+  for (int c = 8; c >= 2; c /= 2)
+    if (tiles256 * c <= sm_count && KB % c == 0 && KB / c >= 16) return c;
+  return 0;
 }
 
 // FP8G_STREAMK=0 turns the stream-K tail off (read on every call).
@@ -1713,8 +1729,14 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
   // small-M variant (64-row A boxes)
   const bool swap = MODE == kDense && !EPI && o.rows <= 64 && env_block_n() == 0 && env_swap_ab();
   if (swap) bn = 64;
-  // cluster K split (opt-in): 256-wide single-CTA tiles, each computed by a cluster of CTAs
-  const int ck_req = (MODE == kDense && !EPI && !swap && !no_alloc) ? env_cluster_k() : 0;
+  // cluster K split: 256-wide single-CTA tiles, each computed by a cluster of CTAs (forced with
+  // FP8G_CLUSTER_K, else chosen for few tiles with a long K, above the small-M shapes)
+  int ck_req = 0;
+  if (MODE == kDense && !EPI && !swap && !no_alloc) {
+    const int ce = env_cluster_k();
+    const int64_t tiles256 = ((o.rows + BM - 1) / BM) * ((o.N + 255) / 256);
+    ck_req = ce >= 0 ? ce : (o.rows > 64 && env_block_n() == 0 && env_pair() == 0 ? cluster_k_auto(tiles256, o.K / BK, dev->sm_count) : 0);
+  }
   if (ck_req > 1) bn = 256;
   // Small-M tiles are 64 wide, or 48 with FP8G_BLOCK_N=48 (other shapes and forms have no 48-wide
   // tiles).  On 64 x 7168 x 7168 the 150 48-wide tiles measured no faster than the 112 64-wide ones

@@ -153,6 +153,24 @@ def test_dense_cluster_k_split(M, N, K, ck, want):
     assert_gemm_close(bf16_to_np(D), gemm_nt(qa, sa, qb, sb), f"cluster K split {M}x{N}x{K} ck={ck}")
 
 
+def test_dense_cluster_k_split_by_default_for_few_tiles_and_long_k():
+    # 128 x 1024 x 16384: four 256-wide tiles and 128 K blocks -- clusters of 8 CTAs by default;
+    # FP8G_CLUSTER_K=0 turns it off; both within the tolerance of the oracle
+    M, N, K = 128, 1024, 16384
+    qa, sa, qb, sb = _problem(M, N, K, seed=123)
+    ref = gemm_nt(qa, sa, qb, sb)
+    with env_var("FP8G_CLUSTER_K", None):
+        D = _dense_gpu(qa, sa, qb, sb)
+        assert g.fp8g_last_config()["cluster_k"] == 8
+    check_status()
+    assert_gemm_close(bf16_to_np(D), ref, "cluster K split by default")
+    with env_var("FP8G_CLUSTER_K", "0"):
+        D0 = _dense_gpu(qa, sa, qb, sb)
+        assert g.fp8g_last_config()["cluster_k"] == 0
+    check_status()
+    assert_gemm_close(bf16_to_np(D0), ref, "cluster K split turned off")
+
+
 def test_dense_swapped_tiles_switch_and_strides():
     # by default M <= 64 takes the 64-wide small-M tiles; strided operands and ld_sa > M in the
     # swapped form (FP8G_SWAP_AB=1)
