@@ -140,6 +140,10 @@ def test_dense_swapped_decode_tiles(M, N, K, split):
     (200, 512, 1024, 2, 2),    # two m-blocks, ragged M
     (100, 2304, 4096, 4, 4),   # ragged N (9 tiles)
     (64, 1024, 1152, 4, 0),    # 9 K blocks: 4 does not divide them, no split
+    (64, 768, 1536, 3, 3),     # clusters of 3, 5, 6 and 7 CTAs (12, 20, 12 and 14 K blocks)
+    (130, 1280, 2560, 5, 5),
+    (96, 512, 1536, 6, 6),
+    (64, 256, 1792, 7, 7),
 ])
 def test_dense_cluster_k_split(M, N, K, ck, want):
     # FP8G_CLUSTER_K: each 256-wide tile's K blocks split over a cluster of CTAs, rank 0 adding the
