@@ -219,24 +219,26 @@ class Case:
         active = int((self.meta > 0).sum())
         return m * w.K + active * w.N * w.K + 4 * (m * kb + active * nbs * kb) + 2 * m * w.N
 
-    def quantize(self, A=None):
+    def quantize(self, A=None, meta=None):
         A = self.A if A is None else A
+        meta = self.meta if meta is None else meta
         if self.w.kind == "masked":  # only each expert's valid rows
             w = self.w
             self.g.fp8_quantize_1x128_masked(A.view(w.E, w.cap, w.K), self.qA.view(w.E, w.cap, w.K), self.sA,
-                                             self.meta)
+                                             meta)
         else:
             self.g.fp8_quantize_1x128(A, self.qA, self.sA)
 
-    def gemm(self, D=None):
+    def gemm(self, D=None, meta=None):
         g, w = self.g, self.w
         D = self.D if D is None else D
+        meta = self.meta if meta is None else meta
         if w.kind == "dense":
             g.fp8_gemm_nt(self.qA, self.sA, self.qB, self.sB, D)
         elif w.kind == "contiguous":
-            g.fp8_grouped_gemm_contiguous(self.qA, self.sA, self.qB, self.sB, D, self.meta)
+            g.fp8_grouped_gemm_contiguous(self.qA, self.sA, self.qB, self.sB, D, meta)
         else:
-            g.fp8_grouped_gemm_masked(self.qA.view(w.E, w.cap, w.K), self.sA, self.qB, self.sB, D, self.meta)
+            g.fp8_grouped_gemm_masked(self.qA.view(w.E, w.cap, w.K), self.sA, self.qB, self.sB, D, meta)
 
 
 # the sources each kernel is built from (a kernel's counters go stale when one of these changes)
@@ -755,53 +757,70 @@ def measure_e2e(cases, g, dev, steps, dist, world):
     """Same metric through the public API with host buffers: pinned bf16 activations (and the
     routing metadata) copied in, the bf16 result copied out, inside the timed region.  As a caller
     would run it: three streams -- copies in, compute (the library's calls), copies out -- so one
-    workload's transfers overlap another's compute; events order each workload's buffers."""
+    workload's transfers overlap another's compute; events order each workload's buffers.  The
+    device-side inputs and results are double-buffered across steps, so the next step's copies in
+    run while this step's results are still computed and copied out (both directions of the host
+    link busy at once)."""
+    nbuf = 2
     host_in = [c.A.cpu().pin_memory() for c in cases]
     host_meta = [c.meta.cpu().pin_memory() if c.meta is not None else None for c in cases]
     host_out = [torch.empty(c.D.shape, dtype=c.D.dtype).pin_memory() for c in cases]
-    dev_in = [torch.empty_like(c.A) for c in cases]
+    dev_in = [[torch.empty_like(c.A) for c in cases] for _ in range(nbuf)]
+    dev_meta = [[torch.empty_like(c.meta) if c.meta is not None else None for c in cases] for _ in range(nbuf)]
+    dev_out = [[torch.empty_like(c.D) for c in cases] for _ in range(nbuf)]
     h2d = sum(t.numel() * t.element_size() for t in host_in) + sum(
         t.numel() * t.element_size() for t in host_meta if t is not None)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in cases]     # inputs of workload i have landed
-    ev_done = [torch.cuda.Event() for _ in cases]   # its GEMM is done (inputs free, result ready)
-    ev_out = [torch.cuda.Event() for _ in cases]    # its result has been copied out (D free)
+    ev_in = [[torch.cuda.Event() for _ in cases] for _ in range(nbuf)]    # inputs of workload i have landed
+    ev_done = [[torch.cuda.Event() for _ in cases] for _ in range(nbuf)]  # its GEMM is done (inputs read, result ready)
+    ev_out = [[torch.cuda.Event() for _ in cases] for _ in range(nbuf)]   # its result has been copied out (D free)
 
-    def step():
-        for i, (c, hi, hm, ho, di) in enumerate(zip(cases, host_in, host_meta, host_out, dev_in)):
+    def step(k):
+        b = k % nbuf
+        for i, (c, hi, hm, ho) in enumerate(zip(cases, host_in, host_meta, host_out)):
+            di, dm, do = dev_in[b][i], dev_meta[b][i], dev_out[b][i]
             with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_done[i])  # the previous step's kernels have read di / meta
+                s_in.wait_event(ev_done[b][i])  # the kernels of the step before last have read di / dm
                 di.copy_(hi, non_blocking=True)
                 if hm is not None:
-                    c.meta.copy_(hm, non_blocking=True)
-                ev_in[i].record(s_in)
+                    dm.copy_(hm, non_blocking=True)
+                ev_in[b][i].record(s_in)
             with torch.cuda.stream(s_comp):
-                s_comp.wait_event(ev_in[i])
-                s_comp.wait_event(ev_out[i])  # the previous step's result has left D
-                c.quantize(di)
-                c.gemm()
-                ev_done[i].record(s_comp)
+                s_comp.wait_event(ev_in[b][i])
+                s_comp.wait_event(ev_out[b][i])  # the result of the step before last has left do
+                c.quantize(di, dm)
+                c.gemm(do, dm)
+                ev_done[b][i].record(s_comp)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_done[i])
-                ho.copy_(c.D, non_blocking=True)
-                ev_out[i].record(s_out)
+                s_out.wait_event(ev_done[b][i])
+                ho.copy_(do, non_blocking=True)
+                ev_out[b][i].record(s_out)
 
-    step()
+    for k in range(nbuf):
+        step(k)
     torch.cuda.synchronize()
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
-    for _ in range(steps):
-        step()
+    for k in range(steps):
+        step(k)
     e1.record(s_out)  # after the last copy out, which follows every other piece of work
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist)
     flops = sum(c.flops for c in cases)
+    # the results copied out equal the device-resident step's (the kernels are deterministic; masked
+    # layout: the rows below each expert's count, the only ones the GEMM writes)
+    def valid(c, t):
+        if c.w.kind != "masked":
+            return t
+        m = c.meta.cpu()
+        return torch.cat([t[e, : int(m[e])] for e in range(c.w.E)])
+    same = all(torch.equal(valid(c, ho), valid(c, c.D.cpu())) for c, ho in zip(cases, host_out))
     return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "results_match_device_step": same,
             "note": "weights resident (quantised once); activations + routing metadata in, bf16 result out; "
-                    "copy-in / compute / copy-out on three streams"}
+                    "copy-in / compute / copy-out on three streams, device buffers double-buffered across steps"}
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
