@@ -242,8 +242,7 @@ class Case:
 
 
 # the sources each kernel is built from (a kernel's counters go stale when one of these changes)
-KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "common.cuh", "quant_math.cuh"),
-                  "quant": ("quantize.cu", "ptx.cuh", "common.cuh", "quant_math.cuh")}
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "common.cuh"), "quant": ("quantize.cu", "ptx.cuh", "common.cuh")}
 
 
 _CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/|\S+', re.S)

@@ -10,7 +10,7 @@
  * Calls (declared below in this order):
  *   quantisation   fp8_quantize_1x128, fp8_quantize_1x128_masked, fp8_route_gather_quantize_1x128,
  *                  fp8_quantize_128x128
- *   GEMMs          fp8_gemm_nt, fp8_quantize_gemm_nt, fp8_gemm_nt_noalloc, fp8_grouped_gemm_contiguous,
+ *   GEMMs          fp8_gemm_nt, fp8_gemm_nt_noalloc, fp8_grouped_gemm_contiguous,
  *                  fp8_grouped_gemm_masked
  *   per-tensor / per-token / per-channel scales
  *                  fp8_quantize_per_row, fp8_quantize_per_tensor, fp8_gemm_nt_scaled,
@@ -19,7 +19,7 @@
  *                  fp8_quantize_1x128_e5m2, fp8_gemm_nt_dgrad, fp8_grouped_gemm_contiguous_dgrad,
  *                  fp8_grouped_gemm_wgrad
  *   status         fp8g_get_status, fp8g_status_string, fp8g_selftest_bounded_waits, fp8g_last_config,
- *                  fp8g_last_split, fp8g_last_swap_ab, fp8g_last_cluster_k, fp8g_last_fused
+ *                  fp8g_last_split, fp8g_last_swap_ab, fp8g_last_cluster_k
  *
  * Sources (page title, section):
  *  - "DeepGEMM FP8 walk-through" (m.czchanglian.com/news/60438), sec. 2.2: per-token
@@ -183,29 +183,6 @@ int fp8_quantize_128x128(const void* w, int64_t E, int64_t N, int64_t K, void* q
 int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t ld_sa, const void* B,
                 int64_t ldb, const float* sB, void* D, int64_t ldd, int64_t M, int64_t N,
                 int64_t K, void* stream);
-
-/*
- * fp8_quantize_gemm_nt -- fp8_quantize_1x128 of the bf16 activations x into A and sA, then
- * fp8_gemm_nt of A and B: the quantised activations are written out as well (a caller can keep
- * them) and D is what the two calls give, bit for bit ("DeepGEMM FP8 walk-through" sec. 2.2:
- * per-token scales of A taken inside the GEMM pipeline; "DeepGEMM explainer" sec. 3.1).
- *
- *   x     bf16 [M, K], row stride ldx elements (ldx >= K, ldx % 8 == 0), 16-byte aligned
- *   A, sA written: e4m3 [M, K] (row stride lda) and fp32 [K/128][ld_sa], as fp8_quantize_1x128
- *   B, sB, D, M, N, K: as fp8_gemm_nt (A's and sA's layout rules included).
- *
- * Decode shapes (M <= 64, the small-M tiles) run as one cooperative launch: every CTA quantises
- * a share of A's 1x128 blocks, all CTAs meet at a grid barrier (two words in the stream's GEMM
- * workspace, made on the first such call on the stream, not inside a stream capture), then the
- * GEMM runs with the first weight stages already loading; fp8g_last_fused reports it.  Other
- * shapes, and calls without a workspace (a first call inside a capture), launch the quantiser
- * and then the GEMM.  The barrier's wait is bounded: if it runs out, FP8G_ERR_TIMEOUT is recorded
- * (fp8g_get_status) and the results are undefined.  Calls on one stream are ordered; calls on
- * different streams use different barriers.  Errors: those of fp8_quantize_1x128 and fp8_gemm_nt.
- */
-int fp8_quantize_gemm_nt(const void* x, int64_t ldx, void* A, int64_t lda, float* sA, int64_t ld_sa,
-                         const void* B, int64_t ldb, const float* sB, void* D, int64_t ldd, int64_t M,
-                         int64_t N, int64_t K, void* stream);
 
 /*
  * fp8_gemm_nt_noalloc -- fp8_gemm_nt that never allocates device memory.  The
@@ -475,13 +452,6 @@ int fp8g_last_swap_ab(int* swapped);
  * Diagnostic only; returns FP8G_OK, or FP8G_ERR_INVALID_ARG for a null pointer.
  */
 int fp8g_last_cluster_k(int* ck);
-
-/*
- * fp8g_last_fused -- 1 when the last GEMM call on this thread was a fp8_quantize_gemm_nt that ran
- * as one launch (quantisation and GEMM fused), else 0.  Diagnostic only; returns FP8G_OK, or
- * FP8G_ERR_INVALID_ARG for a null pointer.
- */
-int fp8g_last_fused(int* fused);
 
 #ifdef __cplusplus
 }

@@ -59,7 +59,6 @@ _SIGNATURES = {
     "fp8_quantize_128x128": [_P, _I64, _I64, _I64, _P, _FP, _P],
     "fp8_gemm_nt": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_gemm_nt_noalloc": [_P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
-    "fp8_quantize_gemm_nt": [_P, _I64, _P, _I64, _FP, _I64, _P, _I64, _FP, _P, _I64, _I64, _I64, _I64, _P],
     "fp8_route_gather_quantize_1x128": [_P, _I64, _I64, _I64, _P, _I32, _I32, _P, _I64, _FP, _I64, _P, _P,
                                         _P, _I64, _P],
     "fp8_grouped_gemm_contiguous": [_P, _FP, _I64, _P, _FP, _P, _P, _I32, _I64, _I64, _I64, _P],
@@ -80,7 +79,6 @@ _SIGNATURES = {
     "fp8g_last_split": [ctypes.POINTER(ctypes.c_int)],
     "fp8g_last_swap_ab": [ctypes.POINTER(ctypes.c_int)],
     "fp8g_last_cluster_k": [ctypes.POINTER(ctypes.c_int)],
-    "fp8g_last_fused": [ctypes.POINTER(ctypes.c_int)],
 }
 
 
@@ -191,23 +189,6 @@ def fp8_gemm_nt(A, sA, B, sB, D) -> None:
     _on_one_device(A, sA, B, sB, D)
     _check(lib().fp8_gemm_nt(_ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B), B.stride(0), _ptr(sB),
                              _ptr(D), D.stride(0), M, N, K, _stream(A)), "fp8_gemm_nt")
-
-
-def fp8_quantize_gemm_nt(x, A, sA, B, sB, D) -> None:
-    """fp8_quantize_1x128(x -> A, sA) then fp8_gemm_nt(A, sA, B, sB -> D); decode shapes (M <= 64)
-    in one launch."""
-    _need(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1, "x: bf16 [M,K], K contiguous")
-    _need(_is_fp8(A) and A.shape == x.shape and A.stride(1) == 1, "A: e4m3 [M,K]")
-    _need(_is_fp8(B) and B.dim() == 2 and B.stride(1) == 1, "B: e4m3 [N,K]")
-    _need(D.dtype == torch.bfloat16 and D.dim() == 2 and D.stride(1) == 1, "D: bf16 [M,N]")
-    M, K = A.shape
-    N = B.shape[0]
-    _need(B.shape[1] == K and D.shape == (M, N), "shapes: x and A [M,K], B [N,K], D [M,N]")
-    ld_sa = _block_scales(sA, sB, M, N, K, 1)
-    _on_one_device(x, A, sA, B, sB, D)
-    _check(lib().fp8_quantize_gemm_nt(_ptr(x), x.stride(0), _ptr(A), A.stride(0), _ptr(sA), ld_sa, _ptr(B),
-                                      B.stride(0), _ptr(sB), _ptr(D), D.stride(0), M, N, K, _stream(x)),
-           "fp8_quantize_gemm_nt")
 
 
 def fp8_gemm_nt_noalloc(A, sA, B, sB, D) -> None:
@@ -424,17 +405,16 @@ def fp8g_get_status(stream: torch.cuda.Stream | None = None) -> int:
 
 def fp8g_last_config() -> dict:
     """Tile width, stages, grid, whether the tail was split (stream-K), whether the tiles were swapped
-    (decode shapes: weight rows on the MMA's M), the cluster size of a cluster K split (0: none) and
-    whether quantisation and GEMM ran as one launch, in this thread's last GEMM."""
+    (decode shapes: weight rows on the MMA's M) and the cluster size of a cluster K split (0: none) in
+    this thread's last GEMM."""
     bn, st, gr, sp, sw = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    ck, fu = ctypes.c_int(), ctypes.c_int()
+    ck = ctypes.c_int()
     _check(lib().fp8g_last_config(ctypes.byref(bn), ctypes.byref(st), ctypes.byref(gr)), "fp8g_last_config")
     _check(lib().fp8g_last_split(ctypes.byref(sp)), "fp8g_last_split")
     _check(lib().fp8g_last_swap_ab(ctypes.byref(sw)), "fp8g_last_swap_ab")
     _check(lib().fp8g_last_cluster_k(ctypes.byref(ck)), "fp8g_last_cluster_k")
-    _check(lib().fp8g_last_fused(ctypes.byref(fu)), "fp8g_last_fused")
     return {"block_n": bn.value, "stages": st.value, "grid": gr.value, "split": bool(sp.value),
-            "swap_ab": bool(sw.value), "cluster_k": ck.value, "fused": bool(fu.value)}
+            "swap_ab": bool(sw.value), "cluster_k": ck.value}
 
 
 # ------------------------------------------------------------------ allocating wrappers

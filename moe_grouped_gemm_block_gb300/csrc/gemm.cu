@@ -50,7 +50,6 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
-#include "quant_math.cuh"
 
 namespace fp8g {
 namespace {
@@ -169,7 +168,7 @@ struct Cfg {
   static constexpr uint32_t kOffSbv = kOffScale + kStages * kScaleStage;
   static constexpr uint32_t kOffX = kOffSbv + kSbvBytes;
   static constexpr uint32_t kOffBar = kOffX + kXBytes;
-  static constexpr uint32_t kNumBars = 3 * kStages + 2 * kTmemBufs + 6;
+  static constexpr uint32_t kNumBars = 3 * kStages + 2 * kTmemBufs + 5;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffTable = kOffMisc + 16;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffOut % 1024 == 0, "alignment");
@@ -227,15 +226,6 @@ struct GemmArgs {
   // cluster K split (see make_work), 0 or 1 when off: each cluster of ck CTAs computes one tile,
   // its ranks taking consecutive K ranges; rank 0 adds the others' partials (workspace slots)
   int32_t ck;
-  // fused quantise-and-multiply (small-M dense form; null fx: off): the kernel first quantises the
-  // bf16 A (fx, row stride ldx) 1x128 into the A operand's memory (fq, row stride ldq) and its scales
-  // into sA, every CTA a share of the blocks, then waits at a grid barrier (fbar: [0] arrivals,
-  // [1] generation; self-resetting) before any of its A or scale reads
-  const __nv_bfloat16* fx;
-  int64_t ldx;
-  uint8_t* fq;
-  int64_t ldq;
-  uint32_t* fbar;
 
   // Test hook, -1 normally: the producer never fills its stage number `test_skip_stage` (counted
   // over the CTA's stages), so the MMA issuer's bounded wait for it runs out and the abort path
@@ -555,10 +545,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
   // (both recomputed from the kernel parameters where used, rather than kept in registers)
   auto ck_in = [&]() { return xfull + 32u + 8u * S; };
   auto ck_on = [&]() { return MODE == kDense && !PAIR && !EPI && a.ck > 1; };
-  // fused quantise-and-multiply: the grid's quantised A and its scales are complete (one arrival,
-  // by the CTA's first promotion thread once it has passed the grid barrier)
-  auto fq_ready = [&]() { return xfull + 40u + 8u * S; };
-  auto fused_on = [&]() { return MODE == kDenseSmallM && !EPI && a.fx != nullptr; };
   constexpr bool kStaged = MODE == kKGrouped;
   // Arrivals that free an operand stage: the MMA commit (lone issuers, CTA pairs and the
   // epilogue-scaled variant); else one lane of the promotion warps once the stage's MMAs have
@@ -589,7 +575,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
     mbar_init(sk_written, C::kEpiWarps);
     mbar_init(sk_ready, 1);
     mbar_init(ck_in(), ck_on() ? static_cast<uint32_t>(a.ck - 1) : 1u);
-    mbar_init(fq_ready(), 1);
     misc[1] = 0;
     misc[2] = 0;  // set when the group table is out of contract
     fence_mbar_init();
@@ -722,19 +707,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
       uint32_t it = 0;  // stages filled
       bool ok = true;
       bool empty_seen = false;  // early test of the next stage's empty barrier (lone form)
-      // Fused quantise-and-multiply: the first S stages get their weights at once and their A
-      // (which this grid is still writing) after the grid barrier, from the deferred list.
-      bool fq_wait = fused_on();
-      uint32_t nd = 0;
-      int32_t d_kb[S], d_row[S];
-      auto issue_deferred = [&]() -> bool {
-        fq_wait = false;
-        if (!wait_bounded(fq_ready(), 0u, a, abort_flag)) return false;
-        fence_proxy_async_global();  // the other CTAs' stores of A, ordered by the barrier
-        for (uint32_t j = 0; j < nd; ++j)
-          tma_load_3d(leader, base + C::kOffA + j * C::kStageABytes, &tmA, full(j), 0, d_row[j], d_kb[j]);
-        return true;
-      };
       Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain, ck_on() ? a.ck : 0);
       Piece pc;
       while (ok && next_piece(w, pc)) {
@@ -742,8 +714,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         if (!fetch_tile(pc, ti)) continue;
         // the K blocks of a stage past the end of K are zero-filled and never read
         for (int32_t kb = pc.kb0; kb < pc.kb1; kb += KPS, ++it) {
-          // every ring slot holds a deferred stage: its A before any slot is reused
-          if (fq_wait && nd == S && !issue_deferred()) { ok = false; break; }
           if (static_cast<int32_t>(it) == a.test_skip_stage) continue;  // test hook (see GemmArgs)
           const uint32_t s = it % S, ph = (it / S) & 1u;
           bool ready;
@@ -762,13 +732,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
             mbar_arrive_expect_tx(leader && rank == 0, full(s), 2 * (C::kStageABytes + C::kStageBBytes));
             tma_load_3d_pair(leader, dA, &tmA, fb, 0, ti.a_row, kb);
             tma_load_4d_pair(leader, dB, &tmB, fb, 0, ti.n0 + static_cast<int32_t>(rank) * C::kBRows, kb, ti.g);
-          } else if (fq_wait) {
-            // stage s == it here (the deferral covers the CTA's first stages only)
-            mbar_arrive_expect_tx(leader, full(s), C::kStageABytes + C::kStageBBytes);
-            tma_load_4d(leader, dB, &tmB, full(s), 0, ti.n0, ti.kb_first + kb, ti.g);
-            d_kb[nd] = ti.kb_first + kb;
-            d_row[nd] = ti.a_row;
-            ++nd;
           } else {
             mbar_arrive_expect_tx(leader, full(s), C::kStageABytes + C::kStageBBytes);
             tma_load_3d(leader, dA, &tmA, full(s), 0, ti.a_row, ti.kb_first + kb);
@@ -783,7 +746,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
           }
         }
       }
-      if (ok && fq_wait && !issue_deferred()) ok = false;  // fewer stages than the ring holds
       if (!ok && leader && rank == 0) {  // let the loads already issued land before the CTA exits
         const uint32_t n = it < S ? it : S;
         for (uint32_t i = it - n; i < it; ++i) {
@@ -1020,76 +982,6 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
     constexpr int kEpiThreads = C::kEpiWarps * 32;
     constexpr int64_t kSlotF4 = static_cast<int64_t>(kEpiThreads) * (C::kEpiCols / 4);
     const int e_thr = ew * 32 + lane;
-    if (fused_on()) {
-      // Fused quantise-and-multiply, first the quantisation: this CTA's share of A's 1x128 blocks,
-      // eight lanes a block (four blocks a warp), with the standalone quantiser's arithmetic, so the
-      // codes and scales are the same bit for bit.
-      constexpr uint32_t kGroups = kEpiThreads / 8;
-      const uint32_t total = static_cast<uint32_t>(a.rows) * static_cast<uint32_t>(a.KB);
-      const uint32_t sub = lane & 7u;
-      float* sa_out = const_cast<float*>(a.sA);
-      for (uint32_t i0 = blockIdx.x * kGroups + static_cast<uint32_t>(ew) * 4u; i0 < total; i0 += gridDim.x * kGroups) {
-        const uint32_t item = i0 + (lane >> 3);
-        const bool live = item < total;
-        const uint32_t m = live ? item / static_cast<uint32_t>(a.KB) : 0u;
-        const uint32_t kbq = live ? item - m * static_cast<uint32_t>(a.KB) : 0u;
-        uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
-        if (live) {
-          const __nv_bfloat16* src = a.fx + static_cast<int64_t>(m) * a.ldx + kbq * 128u + sub * 8u;
-          r0 = __ldg(reinterpret_cast<const uint4*>(src));
-          r1 = __ldg(reinterpret_cast<const uint4*>(src + 64));
-        }
-        float f[16], lo[8], hi[8];
-        unpack8(r0, lo);
-        unpack8(r1, hi);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          f[i] = lo[i];
-          f[8 + i] = hi[i];
-        }
-        float amax = fmaxf(amax8(lo), amax8(hi));
-#pragma unroll
-        for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float sq = block_scale<kE4M3>(amax);
-        if (live) {
-          uint32_t c[4];
-          quant_n<16, kE4M3>(f, sq, direct_mode(amax, sq), c);
-          uint8_t* dst = a.fq + static_cast<int64_t>(m) * a.ldq + kbq * 128u + sub * 8u;
-          *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
-          *reinterpret_cast<uint2*>(dst + 64) = make_uint2(c[2], c[3]);
-          if (sub == 0) sa_out[static_cast<int64_t>(kbq) * a.ld_sa + m] = sq;
-        }
-      }
-      // Then the grid barrier (every CTA is resident: a cooperative launch).  The promotion warps'
-      // stores are ordered before one thread's arrival by a barrier among them and a GPU-scope
-      // fence; the last CTA to arrive resets the count and moves the generation on.
-      named_bar_sync(1, kEpiThreads);
-      if (ew == 0 && lane == 0) {
-        uint32_t* cnt = a.fbar;
-        uint32_t* gen = a.fbar + 1;
-        const uint32_t g0 = ld_acquire_gpu(gen);
-        __threadfence();
-        if (atomicAdd(cnt, 1u) == gridDim.x - 1u) {
-          atomicExch(cnt, 0u);
-          __threadfence();
-          st_release_gpu(gen, g0 + 1u);
-        } else {
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(gen) == g0) {
-            if (*abort_flag) break;
-            if (clock64() - t0 > a.budget) {
-              *abort_flag = 1;
-              record_status(a.status, FP8G_ERR_TIMEOUT);
-              break;
-            }
-            __nanosleep(32);
-          }
-        }
-        mbar_arrive(fq_ready());  // also after a timeout: the others then see the abort flag
-      }
-      // the scale reads below (through L2: other CTAs wrote them) follow the barrier
-      if (!__all_sync(0xffffffffu, wait_bounded(fq_ready(), 0u, a, abort_flag)) || *abort_flag) ok = false;
-    }
     Work w = make_work(num_tiles, tile_step, tile0, a.KB, sk_on, a.sk_min_units, a.sk_min_gain, ck_on() ? a.ck : 0);
     Piece pc;
     while (ok && next_piece(w, pc)) {
@@ -1198,11 +1090,7 @@ __global__ void __launch_bounds__(CfgOf<BN, MODE, PAIR>::kThreads, 1)
         const int32_t cut = kTwoSb ? 128 - ncol0 % 128 : C::kEpiCols;
         const bool has_hi = kTwoSb && cut < C::kEpiCols && ncol0 / 128 + 1 < a.NBs;
         auto load_scales = [&](int32_t kbi, float& sa_o, float& sb_o, float& sbh_o) {
-          // (small-M tiles read through L2: the fused form writes sA in this kernel)
-          if constexpr (MODE == kDenseSmallM)
-            sa_o = ld_cg_f32_or0(sap + static_cast<int64_t>(kbi) * a.ld_sa, row_ok && kbi < pc.kb1);
-          else
-            sa_o = ld_nc_f32_or0(sap + static_cast<int64_t>(kbi) * a.ld_sa, MODE != kKGrouped && row_ok && kbi < pc.kb1);
+          sa_o = ld_nc_f32_or0(sap + static_cast<int64_t>(kbi) * a.ld_sa, MODE != kKGrouped && row_ok && kbi < pc.kb1);
           sb_o = ld_nc_f32_or0(sbp + kbi, blk_sb && kbi < pc.kb1);
           sbh_o = kTwoSb ? ld_nc_f32_or0(sbp + a.KB + kbi, blk_sb && has_hi && kbi < pc.kb1) : 0.0f;
         };
@@ -1614,10 +1502,9 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
     }
     return FP8G_OK;
   }
-  if (args.sk || args.fx) {
-    // stream-K: a CTA finishing a split tile waits for other CTAs' partials; fused
-    // quantise-and-multiply: every CTA waits at the grid barrier.  So every CTA must be resident at
-    // once -- a cooperative launch guarantees it (one CTA per SM, grid <= SMs)
+  if (args.sk) {
+    // stream-K: a CTA finishing a split tile waits for other CTAs' partials, so every CTA must
+    // be resident at once -- a cooperative launch guarantees it (one CTA per SM, grid <= SMs)
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(C::kThreads);
@@ -1659,9 +1546,6 @@ int launch_kernel(const GemmArgs& args, const CUtensorMap& tA, const CUtensorMap
 // partial-tile slot per SM (kSkSlotBytes: 128 x 128 columns x 2 column groups at most) and one
 // flag per SM.
 static_assert(kSkSlotBytes == static_cast<size_t>(BM) * 256 * 4, "stream-K slot size");
-// The fused form's two grid barrier words follow the per-SM flags, 8-byte aligned.
-size_t grid_bar_word(int sm_count) { return (static_cast<size_t>(sm_count) + 1) / 2 * 2; }
-
 struct SkWorkspace {
   void* base = nullptr;
   size_t flag_offset = 0;
@@ -1672,8 +1556,7 @@ std::map<std::pair<int, cudaStream_t>, SkWorkspace>* g_sk_ws = nullptr;
 // The workspace of (device, stream), or false when there is none and it cannot be made now
 // (allocation failed, or the stream is being captured into a graph: no allocation inside a
 // capture -- the call then runs without the stream-K tail).
-bool sk_workspace(int dev, int sm_count, cudaStream_t stream, float4** part, uint32_t** flags,
-                  uint32_t** grid_bar = nullptr) {
+bool sk_workspace(int dev, int sm_count, cudaStream_t stream, float4** part, uint32_t** flags) {
   std::lock_guard<std::mutex> lock(g_sk_mutex);
   if (!g_sk_ws) g_sk_ws = new std::map<std::pair<int, cudaStream_t>, SkWorkspace>();
   SkWorkspace& w = (*g_sk_ws)[{dev, stream}];
@@ -1684,17 +1567,10 @@ bool sk_workspace(int dev, int sm_count, cudaStream_t stream, float4** part, uin
       return false;
     }
     const size_t part_bytes = kSkSlotBytes * static_cast<size_t>(sm_count);
-    // one flag per SM (zeroed before each split launch), then the fused form's grid barrier words
-    // (arrivals, generation: self-resetting, zeroed once here)
-    const size_t flag_bytes = (grid_bar_word(sm_count) * 4 + 8 + 255) / 256 * 256;
+    const size_t flag_bytes = (static_cast<size_t>(sm_count) * 4 + 255) / 256 * 256;
     void* p = nullptr;
     if (cudaMalloc(&p, part_bytes + flag_bytes) != cudaSuccess) {
       cudaGetLastError();
-      return false;
-    }
-    if (cudaMemsetAsync(static_cast<char*>(p) + part_bytes, 0, flag_bytes, stream) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(p);
       return false;
     }
     w.base = p;
@@ -1702,7 +1578,6 @@ bool sk_workspace(int dev, int sm_count, cudaStream_t stream, float4** part, uin
   }
   *part = static_cast<float4*>(w.base);
   *flags = reinterpret_cast<uint32_t*>(static_cast<char*>(w.base) + w.flag_offset);
-  if (grid_bar) *grid_bar = *flags + grid_bar_word(sm_count);
   return true;
 }
 
@@ -1777,7 +1652,6 @@ bool env_streamk() {
 
 thread_local int t_last_bn = 0, t_last_stages = 0, t_last_grid = 0, t_last_split = 0, t_last_swap = 0;
 thread_local int t_last_ck = 0;
-thread_local int t_last_fused = 0;
 
 // FP8G_PAIR=1 runs 256-wide tiles as 256 x 256 CTA-pair tiles, FP8G_PAIR=2 as 256 x 128 pair
 // tiles (four TMEM partial buffers per CTA).  Off by default: measured no faster than single-CTA
@@ -1834,8 +1708,6 @@ struct Operands {
   int32_t sa_step = 0, sb_step = 0;  // epilogue-scaled variant only
   uint32_t idesc_fmt = 0;             // operand formats (A e5m2: 1 << 7)
   int64_t ld_sb = 0;                  // kKGrouped: B scales [K blocks][ld_sb]
-  const void* fx = nullptr;           // bf16 A to quantise first into A / sA (fp8_quantize_gemm_nt)
-  int64_t ldx = 0;
 };
 
 // EPI: the epilogue-scaled variant (per-tensor / per-token / per-channel scales)
@@ -2053,34 +1925,6 @@ int run_gemm(const Operands& o, cudaStream_t stream, bool no_alloc = false) {
     if (MODE != kDense) table_entries = 2 * static_cast<int>(o.E + 1);
   }
 
-  // fp8_quantize_gemm_nt: small-M tiles quantise A in the same launch (grid barrier in the
-  // workspace of this stream); any other form quantises first with the standalone quantiser
-  bool fused = false;
-  if constexpr (MODE == kDense && !EPI) {
-    if (o.fx) {
-      if (small_m && a.ck <= 1 && !no_alloc) {
-        int dev_id = 0;
-        cudaGetDevice(&dev_id);
-        float4* part = nullptr;
-        uint32_t* flags = nullptr;
-        uint32_t* gbar = nullptr;
-        if (sk_workspace(dev_id, dev->sm_count, stream, &part, &flags, &gbar)) {
-          a.fx = static_cast<const __nv_bfloat16*>(o.fx);
-          a.ldx = o.ldx;
-          a.fq = static_cast<uint8_t*>(const_cast<void*>(o.A));
-          a.ldq = o.lda;
-          a.fbar = gbar;
-          fused = true;
-        }
-      }
-      if (!fused) {
-        const int qs = fp8_quantize_1x128(o.fx, o.rows, o.K, o.ldx, const_cast<void*>(o.A), o.lda,
-                                          const_cast<float*>(o.sA), o.ld_sa, stream);
-        if (qs != FP8G_OK) return qs;
-      }
-    }
-  }
-  t_last_fused = fused ? 1 : 0;
   t_last_bn = bn;
   t_last_grid = grid;
   t_last_split = a.sk;
@@ -2169,26 +2013,6 @@ extern "C" int fp8_gemm_nt(const void* A, int64_t lda, const float* sA, int64_t 
       lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0 || ld_sa % 4 != 0)
     return FP8G_ERR_ALIGNMENT;
   Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr};
-  return run_gemm<kDense>(o, static_cast<cudaStream_t>(stream));
-}
-
-extern "C" int fp8_quantize_gemm_nt(const void* x, int64_t ldx, void* A, int64_t lda, float* sA,
-                                    int64_t ld_sa, const void* B, int64_t ldb, const float* sB, void* D,
-                                    int64_t ldd, int64_t M, int64_t N, int64_t K, void* stream) {
-  // the argument rules of fp8_quantize_1x128 (x) and of fp8_gemm_nt (the rest)
-  if (M < 0 || M > kMaxI32 || N <= 0 || N > kMaxI32 || N % 16 != 0 || K <= 0 || K % 128 != 0 ||
-      K > kMaxI32)
-    return FP8G_ERR_INVALID_ARG;
-  if (ldx < K || lda < K || ldb < K || ldd < N || ld_sa < M) return FP8G_ERR_INVALID_ARG;
-  if (M == 0) return FP8G_OK;
-  if (!x || !A || !sA || !B || !sB || !D) return FP8G_ERR_INVALID_ARG;
-  if (M * (K / 128) >= (int64_t{1} << 31)) return FP8G_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(A) || !aligned16(sA) || !aligned16(B) || !aligned16(sB) || !aligned16(D) ||
-      ldx % 8 != 0 || lda % 16 != 0 || ldb % 16 != 0 || ldd % 8 != 0 || ld_sa % 4 != 0)
-    return FP8G_ERR_ALIGNMENT;
-  Operands o{A, lda, sA, ld_sa, B, ldb, sB, D, ldd, M, N, K, 1, 0, nullptr};
-  o.fx = x;
-  o.ldx = ldx;
   return run_gemm<kDense>(o, static_cast<cudaStream_t>(stream));
 }
 
@@ -2401,12 +2225,6 @@ extern "C" int fp8g_last_swap_ab(int* swapped) {
 extern "C" int fp8g_last_cluster_k(int* ck) {
   if (!ck) return FP8G_ERR_INVALID_ARG;
   *ck = t_last_ck;
-  return FP8G_OK;
-}
-
-extern "C" int fp8g_last_fused(int* fused) {
-  if (!fused) return FP8G_ERR_INVALID_ARG;
-  *fused = t_last_fused;
   return FP8G_OK;
 }
 

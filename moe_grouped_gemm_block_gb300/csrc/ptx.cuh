@@ -386,28 +386,6 @@ __device__ __forceinline__ float ld_nc_f32_or0(const float* p, bool pred) {
   return v;
 }
 
-// 0 when !pred, else the value at p through L2 (coherent: for data other CTAs of the same kernel
-// wrote before a grid barrier)
-__device__ __forceinline__ float ld_cg_f32_or0(const float* p, bool pred) {
-  float v;
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\tmov.b32 %0, 0;\n\t@q ld.global.cg.f32 %0, [%1];\n\t}"
-      : "=f"(v)
-      : "l"(p), "r"(static_cast<uint32_t>(pred)));
-  return v;
-}
-
-// A barrier among `count` threads of the CTA (warps that reach it), id 1..15 (0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Lets TMA (the async proxy) see global data that ordinary stores of other threads wrote, once a
-// barrier has ordered those stores before this thread.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ float ld_nc_f32(const float* p) {
   float v;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));

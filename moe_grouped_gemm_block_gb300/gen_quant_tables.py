@@ -1,5 +1,5 @@
 """Generator of the quantiser's direct-path table (build helper; its output is pasted into
-csrc/quant_math.cuh as kDirectMode0..7 and a CPU test checks the two agree).
+csrc/quantize.cu as kDirectMode0..7 and a CPU test checks the two agree).
 
 The quantisers compute e4m3(RN(x / s)) with s = RN(amax / 448).  For most blocks a single product
 y = RN(x * r) with a fixed multiplier r already has the same e4m3 code for every bf16 x with

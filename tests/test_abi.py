@@ -104,7 +104,6 @@ def test_last_config_null_pointer(lib):
     assert lib.fp8g_last_split(null) == INVALID
     assert lib.fp8g_last_swap_ab(null) == INVALID
     assert lib.fp8g_last_cluster_k(null) == INVALID
-    assert lib.fp8g_last_fused(null) == INVALID
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):
@@ -121,27 +120,6 @@ def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):
 def test_gemm_nt_noalloc_validation(lib, kw, want):
     # the fixed-scratch variant takes fp8_gemm_nt's arguments and rules
     assert lib.fp8_gemm_nt_noalloc(*_nt(**kw)) == want
-
-
-def _qnt(**kw):
-    a = dict(x=P, ldx=256, A=P, lda=256, sA=P, ld_sa=64, B=P, ldb=256, sB=P, D=P, ldd=256, M=64, N=256, K=256,
-             s=None)
-    a.update(kw)
-    return tuple(a.values())
-
-
-@pytest.mark.parametrize("kw,want", [
-    (dict(K=200), INVALID), (dict(N=250), INVALID), (dict(M=-1), INVALID), (dict(ldx=128), INVALID),
-    (dict(lda=128), INVALID), (dict(ld_sa=32), INVALID), (dict(x=None), INVALID), (dict(sA=None), INVALID),
-    (dict(x=P + 2), ALIGN), (dict(ldx=260), ALIGN), (dict(A=P + 1), ALIGN), (dict(ldd=260), ALIGN),
-])
-def test_quantize_gemm_nt_validation(lib, kw, want):
-    # the quantiser's rules for x, fp8_gemm_nt's for the rest
-    assert lib.fp8_quantize_gemm_nt(*_qnt(**kw)) == want
-
-
-def test_quantize_gemm_nt_m_zero_is_a_noop(lib):
-    assert lib.fp8_quantize_gemm_nt(*_qnt(M=0, x=None, A=None, sA=None, B=None, sB=None, D=None)) == 0
 
 
 def test_gemm_nt_noalloc_m_zero_is_a_noop(lib):

@@ -1,4 +1,4 @@
-"""The quantiser's direct-path table (kDirectMode0..7 in csrc/quant_math.cuh), checked without a GPU.
+"""The quantiser's direct-path table (kDirectMode0..7 in csrc/quantize.cu), checked without a GPU.
 
 For an amax whose 8-bit bf16 significand A has a non-zero mode, the kernel takes the e4m3 code of the
 single product RN(x * r) instead of its bracketing test, with r = RN(1/s) (mode 1), one ulp above
@@ -18,7 +18,7 @@ import pytest
 from oracle.e4m3 import e4m3_encode
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-QUANT_CU = os.path.join(ROOT, "moe_grouped_gemm_block_gb300", "csrc", "quant_math.cuh")
+QUANT_CU = os.path.join(ROOT, "moe_grouped_gemm_block_gb300", "csrc", "quantize.cu")
 STEP = {1: 0, 2: 1, 3: -1}
 
 
