@@ -197,6 +197,9 @@ class Case:
         elif w.kind == "contiguous":
             self.D = torch.empty((self.rows, w.N), dtype=torch.bfloat16, device=dev)
             self.meta = inp["group_offsets"].to(dev)
+            # what a caller holds before routing: the tokens and the router's choices
+            self.tokens = inp["tokens"]
+            self.topk_ids = inp["topk_ids"]
         else:
             self.D = torch.empty((w.E, w.cap, w.N), dtype=torch.bfloat16, device=dev)
             self.meta = inp["masked_m"].to(dev)
@@ -754,47 +757,114 @@ def measure_scaled_rows(g, dev, flush, hbm_peak, fp8_peak, reps):
 
 
 def measure_e2e(cases, g, dev, steps, dist, world):
-    """Same metric through the public API with host buffers: pinned bf16 activations (and the
-    routing metadata) copied in, the bf16 result copied out, inside the timed region.  As a caller
-    would run it: three streams -- copies in, compute (the library's calls), copies out -- so one
-    workload's transfers overlap another's compute; events order each workload's buffers.  The
-    device-side inputs and results are double-buffered across steps, so the next step's copies in
-    run while this step's results are still computed and copied out (both directions of the host
-    link busy at once)."""
+    """Same metric through the public API with host buffers: inside the timed region, every step
+    copies in from pinned host memory what a caller holds and copies the bf16 results out.
+      - dense: the activations in, D out;
+      - MoE contiguous: the tokens and the router's top-k expert ids in; the routed layout is built
+        and quantised on the device (fp8_route_gather_quantize_1x128), then the grouped GEMM; the
+        routed rows of D out;
+      - MoE masked: each expert's valid rows in (one copy per expert), and the same rows of D out.
+    Three streams -- copies in, compute (the library's calls), copies out -- so one workload's
+    transfers overlap another's compute, with the device-side inputs and results double-buffered
+    across steps; events order each workload's buffers."""
     nbuf = 2
-    host_in = [c.A.cpu().pin_memory() for c in cases]
-    host_meta = [c.meta.cpu().pin_memory() if c.meta is not None else None for c in cases]
-    host_out = [torch.empty(c.D.shape, dtype=c.D.dtype).pin_memory() for c in cases]
-    dev_in = [[torch.empty_like(c.A) for c in cases] for _ in range(nbuf)]
-    dev_meta = [[torch.empty_like(c.meta) if c.meta is not None else None for c in cases] for _ in range(nbuf)]
-    dev_out = [[torch.empty_like(c.D) for c in cases] for _ in range(nbuf)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in) + sum(
-        t.numel() * t.element_size() for t in host_meta if t is not None)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    plans = []
+    for c in cases:
+        w = c.w
+        p = {"c": c}
+        if w.kind == "contiguous":
+            T, topk = c.topk_ids.shape
+            m_cap = g.route_capacity(T, topk, w.E)
+            used = int(c.meta[-1])
+            p.update(route=True, m_cap=m_cap, used=used,
+                     host_in=[c.tokens.cpu().pin_memory(), c.topk_ids.contiguous().pin_memory()],
+                     host_out=torch.empty((used, w.N), dtype=torch.bfloat16).pin_memory())
+            p["dev_in"] = [[torch.empty_like(t, device=dev) for t in p["host_in"]] for _ in range(nbuf)]
+            p["dev_out"] = [torch.empty((m_cap, w.N), dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+            p["q"] = torch.empty((m_cap, w.K), dtype=torch.uint8, device=dev)
+            p["sA"] = torch.empty((w.K // 128, m_cap), dtype=torch.float32, device=dev)
+            p["offs"] = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+            p["row_token"] = torch.empty(m_cap, dtype=torch.int32, device=dev)
+            p["entry_row"] = torch.empty((T, topk), dtype=torch.int32, device=dev)
+            p["in_bytes"] = sum(t.numel() * t.element_size() for t in p["host_in"])
+            p["out_bytes"] = used * w.N * 2
+        elif w.kind == "masked":
+            counts = [int(v) for v in c.meta.cpu()]
+            p.update(route=False, counts=counts, host_in=[c.A.view(w.E, w.cap, w.K).cpu().pin_memory(),
+                                                          c.meta.cpu().pin_memory()],
+                     host_out=torch.empty(c.D.shape, dtype=c.D.dtype).pin_memory())
+            p["dev_in"] = [[torch.empty_like(t, device=dev) for t in p["host_in"]] for _ in range(nbuf)]
+            p["dev_out"] = [torch.empty_like(c.D) for _ in range(nbuf)]
+            p["in_bytes"] = sum(counts) * w.K * 2 + w.E * 4
+            p["out_bytes"] = sum(counts) * w.N * 2
+        else:
+            p.update(route=False, host_in=[c.A.cpu().pin_memory()],
+                     host_out=torch.empty(c.D.shape, dtype=c.D.dtype).pin_memory())
+            p["dev_in"] = [[torch.empty_like(c.A)] for _ in range(nbuf)]
+            p["dev_out"] = [torch.empty_like(c.D) for _ in range(nbuf)]
+            p["in_bytes"] = c.A.numel() * 2
+            p["out_bytes"] = c.D.numel() * 2
+        plans.append(p)
+    h2d = sum(p["in_bytes"] for p in plans)
+    d2h = sum(p["out_bytes"] for p in plans)
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [[torch.cuda.Event() for _ in cases] for _ in range(nbuf)]    # inputs of workload i have landed
     ev_done = [[torch.cuda.Event() for _ in cases] for _ in range(nbuf)]  # its GEMM is done (inputs read, result ready)
     ev_out = [[torch.cuda.Event() for _ in cases] for _ in range(nbuf)]   # its result has been copied out (D free)
 
+    def copy_in(p, b):
+        c, w, hs, ds = p["c"], p["c"].w, p["host_in"], p["dev_in"][b]
+        if w.kind == "masked":
+            for e, n in enumerate(p["counts"]):
+                if n:
+                    ds[0][e, :n].copy_(hs[0][e, :n], non_blocking=True)
+            ds[1].copy_(hs[1], non_blocking=True)
+        else:
+            for d, h in zip(ds, hs):
+                d.copy_(h, non_blocking=True)
+
+    def compute(p, b):
+        c, w, ds, do = p["c"], p["c"].w, p["dev_in"][b], p["dev_out"][b]
+        if p["route"]:
+            g.fp8_route_gather_quantize_1x128(ds[0], ds[1], w.E, p["q"], p["sA"], p["offs"], p["row_token"],
+                                              p["entry_row"])
+            # M_total = the routed rows (known to the host, which routed): the device step's launch
+            # configuration, so the same tail split and the same summation order
+            u = p["used"]
+            g.fp8_grouped_gemm_contiguous(p["q"][:u], p["sA"], c.qB, c.sB, do[:u], p["offs"])
+        elif w.kind == "masked":
+            c.quantize(ds[0].view(-1, w.K), ds[1])
+            c.gemm(do, ds[1])
+        else:
+            c.quantize(ds[0])
+            c.gemm(do)
+
+    def copy_out(p, b):
+        c, w, ho, do = p["c"], p["c"].w, p["host_out"], p["dev_out"][b]
+        if p["route"]:
+            ho.copy_(do[: p["used"]], non_blocking=True)
+        elif w.kind == "masked":
+            for e, n in enumerate(p["counts"]):
+                if n:
+                    ho[e, :n].copy_(do[e, :n], non_blocking=True)
+        else:
+            ho.copy_(do, non_blocking=True)
+
     def step(k):
         b = k % nbuf
-        for i, (c, hi, hm, ho) in enumerate(zip(cases, host_in, host_meta, host_out)):
-            di, dm, do = dev_in[b][i], dev_meta[b][i], dev_out[b][i]
+        for i, p in enumerate(plans):
             with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_done[b][i])  # the kernels of the step before last have read di / dm
-                di.copy_(hi, non_blocking=True)
-                if hm is not None:
-                    dm.copy_(hm, non_blocking=True)
+                s_in.wait_event(ev_done[b][i])  # the kernels of the step before last have read this set
+                copy_in(p, b)
                 ev_in[b][i].record(s_in)
             with torch.cuda.stream(s_comp):
                 s_comp.wait_event(ev_in[b][i])
-                s_comp.wait_event(ev_out[b][i])  # the result of the step before last has left do
-                c.quantize(di, dm)
-                c.gemm(do, dm)
+                s_comp.wait_event(ev_out[b][i])  # the result of the step before last has been copied out
+                compute(p, b)
                 ev_done[b][i].record(s_comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[b][i])
-                ho.copy_(do, non_blocking=True)
+                copy_out(p, b)
                 ev_out[b][i].record(s_out)
 
     for k in range(nbuf):
@@ -809,18 +879,24 @@ def measure_e2e(cases, g, dev, steps, dist, world):
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, dist)
     flops = sum(c.flops for c in cases)
-    # the results copied out equal the device-resident step's (the kernels are deterministic; masked
-    # layout: the rows below each expert's count, the only ones the GEMM writes)
-    def valid(c, t):
-        if c.w.kind != "masked":
-            return t
-        m = c.meta.cpu()
-        return torch.cat([t[e, : int(m[e])] for e in range(c.w.E)])
-    same = all(torch.equal(valid(c, ho), valid(c, c.D.cpu())) for c, ho in zip(cases, host_out))
+
+    # the results copied out equal the device-resident step's bit for bit (deterministic kernels;
+    # the routed layout is the one the host built for that step)
+    def same(p):
+        c, w, ho = p["c"], p["c"].w, p["host_out"]
+        ref = c.D.cpu()
+        if p["route"]:
+            return torch.equal(ho, ref[: p["used"]])
+        if w.kind == "masked":
+            return all(torch.equal(ho[e, :n], ref[e, :n]) for e, n in enumerate(p["counts"]))
+        return torch.equal(ho, ref)
     return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "results_match_device_step": same,
-            "note": "weights resident (quantised once); activations + routing metadata in, bf16 result out; "
-                    "copy-in / compute / copy-out on three streams, device buffers double-buffered across steps"}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "results_match_device_step": {p["c"].name: same(p) for p in plans},
+            "note": "weights resident (quantised once); in: activations (MoE contiguous: tokens + top-k ids, "
+                    "routed and quantised on the device; masked: each expert's valid rows), out: the bf16 "
+                    "result rows; copy-in / compute / copy-out on three streams, device buffers "
+                    "double-buffered across steps"}
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)

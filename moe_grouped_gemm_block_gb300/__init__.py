@@ -438,6 +438,30 @@ def route_capacity(T: int, topk: int, E: int) -> int:
     return round_up(T * topk + 127 * E, 128)
 
 
+def fp8_route_gather_quantize_1x128(x, topk_ids, E, q, sA, group_offsets, row_token, entry_row) -> None:
+    """The routed layout into caller buffers: tokens x bf16 [T,K], topk_ids int32 [T,topk] ->
+    q uint8 [M_cap,K], sA f32 [K/128, ld_sa >= M_cap], group_offsets int32 [E+1], row_token int32
+    [M_cap], entry_row int32 [T,topk] (all on the device)."""
+    _need(x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1, "x: bf16 [T,K], K contiguous")
+    T, K = x.shape
+    _need(topk_ids.dtype == torch.int32 and topk_ids.dim() == 2 and topk_ids.shape[0] == T
+          and topk_ids.is_contiguous(), "topk_ids: int32 [T,topk] contiguous")
+    topk = topk_ids.shape[1]
+    m = q.shape[0]
+    _need(_is_fp8(q) and q.dim() == 2 and q.shape[1] == K and q.stride(1) == 1, "q: e4m3 [M_cap,K]")
+    _need(sA.dtype == torch.float32 and sA.dim() == 2 and sA.shape[0] == K // 128 and sA.stride(1) == 1
+          and sA.shape[1] >= m, "sA: f32 [K/128, ld_sa >= M_cap]")
+    _need(group_offsets.dtype == torch.int32 and group_offsets.numel() == E + 1, "group_offsets: int32 [E+1]")
+    _need(row_token.dtype == torch.int32 and row_token.numel() == m, "row_token: int32 [M_cap]")
+    _need(entry_row.dtype == torch.int32 and entry_row.shape == topk_ids.shape and entry_row.is_contiguous(),
+          "entry_row: int32 [T,topk]")
+    _on_one_device(x, topk_ids, q, sA, group_offsets, row_token, entry_row)
+    _check(lib().fp8_route_gather_quantize_1x128(_ptr(x), T, K, x.stride(0), _ptr(topk_ids), topk, E, _ptr(q),
+                                                 q.stride(0), _ptr(sA), sA.stride(0), _ptr(group_offsets),
+                                                 _ptr(row_token), _ptr(entry_row), m, _stream(x)),
+           "fp8_route_gather_quantize_1x128")
+
+
 def route_gather_quantize_1x128(x: torch.Tensor, topk_ids: torch.Tensor, E: int, m_cap: int | None = None):
     """bf16 tokens [T,K] + int32 expert choices [T,topk] (device) -> (q uint8 [m_cap,K],
     sA f32 [K/128, m_cap], group_offsets int32 [E+1], row_token int32 [m_cap],
