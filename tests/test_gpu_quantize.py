@@ -172,7 +172,12 @@ def test_1x128_every_amax_significand_against_every_x():
     _check_1x128(xt)
 
 
-@pytest.mark.parametrize("E,cap,K", [(5, 256, 512), (3, 16, 128), (32, 256, 7168)])
+@pytest.mark.parametrize("E,cap,K", [
+    (5, 256, 512), (3, 16, 128), (32, 256, 7168),
+    (40, 48, 384),     # three K blocks a row: groups of a warp leave the item loop at different passes
+    (1024, 16, 256),   # many experts, one grid row each
+    (1100, 16, 256),
+])
 def test_masked_rows_quantiser(E, cap, K):
     # only rows m < masked_m[e] are quantised (counts clamped to [0, cap]); the rest keep their bytes
     import moe_grouped_gemm_block_gb300 as g
