@@ -1596,7 +1596,8 @@ int env_test_skip_stage() {
 //   streams once per band.
 //   Contiguous-grouped: 8 m-blocks.  A band spanning every expert keeps all experts' B column blocks
 //   in flight at once (the grouped data gradient, 8576 x 7168 x 4096: 248 us with all 67 m-blocks,
-//   226 us with 8 or 16; the MoE forward GEMM: 231 us with 8, 236 us with 16).
+//   226 us with 8 or 16; the MoE forward GEMM: 231 us with 8, 236 us with 16; again with the current
+//   kernel: 220-221 us with 8, 224 with 4, 225 with 6, 230 with 10, 223 with 12, 221 with 16).
 //   K-grouped: 16.
 // FP8G_BAND_M overrides (read on every call).
 int32_t band_rows(int32_t num_m, int64_t K, int mode) {
